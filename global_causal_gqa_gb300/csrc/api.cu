@@ -1,0 +1,224 @@
+// api.cu -- the extern "C" entry points declared in gqa_attn.h.
+//
+// Host-side argument checks, the per-device status word, and launches on the caller's
+// stream.  No entry point allocates memory or synchronises, except
+// gqa_get_device_status (which synchronises the given stream to read the status word).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "gqa_attn.h"
+#include "internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// One status word per device.  Kernels record the first device-side error here with
+// atomicCAS; gqa_get_device_status reads and clears it.
+__device__ int g_status_word;
+
+int *status_ptr() {
+    static std::mutex mu;
+    static int *ptrs[kMaxDevices] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int *>(p);
+    }
+    return ptrs[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool rope_dim_ok(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
+
+gqa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+gqa_status gqa_rope_inv_freq(double *out, int d, double base, double yarn_factor,
+                             double yarn_L0, double beta_fast, double beta_slow,
+                             double rotate_fraction) {
+    if (!out || d <= 0 || (d % 2) != 0 || !(base > 1.0) || !(yarn_factor >= 1.0) ||
+        !(rotate_fraction > 0.0 && rotate_fraction <= 1.0))
+        return GQA_ERR_INVALID_ARG;
+    const int half = d / 2;
+    const bool yarn = yarn_factor != 1.0;
+    double lo = 0.0, hi = 1.0;
+    if (yarn) {
+        if (!(yarn_L0 > 0.0) || !(beta_fast > 0.0) || !(beta_slow > 0.0) || beta_fast == beta_slow)
+            return GQA_ERR_INVALID_ARG;
+        const double two_pi = 6.283185307179586476925286766559;
+        lo = half * std::log(yarn_L0 / (two_pi * beta_fast)) / std::log(base);
+        hi = half * std::log(yarn_L0 / (two_pi * beta_slow)) / std::log(base);
+    }
+    const int rotated = rotate_fraction < 1.0
+                            ? static_cast<int>(std::floor(rotate_fraction * half + 0.5))
+                            : half;
+    for (int j = 0; j < half; ++j) {
+        double w = std::pow(base, -2.0 * j / d);
+        if (yarn) {
+            double a = (j - lo) / (hi - lo);
+            a = a < 0.0 ? 0.0 : (a > 1.0 ? 1.0 : a);
+            w *= (1.0 - a) + a / yarn_factor;
+        }
+        out[j] = j < rotated ? w : 0.0;
+    }
+    return GQA_OK;
+}
+
+double gqa_yarn_amplitude(double s) { return 1.0 + 0.1 * std::log(s); }
+
+size_t gqa_rope_table_bytes(int d, int max_pos) {
+    if (d <= 0 || max_pos <= 0) return 0;
+    return static_cast<size_t>(max_pos) * (d / 2) * 2 * sizeof(float);
+}
+
+gqa_status gqa_rope_table_build(float *table, const double *inv_freq, int d, double amp,
+                                int max_pos, gqa_stream_t stream) {
+    if (!table || !inv_freq || !rope_dim_ok(d) || max_pos <= 0 || !std::isfinite(amp))
+        return GQA_ERR_INVALID_ARG;
+    if (!aligned16(table)) return GQA_ERR_ALIGNMENT;
+    gqa::InvFreq w{};
+    for (int j = 0; j < d / 2; ++j) w.w[j] = inv_freq[j];
+    return from_cuda(gqa::launch_rope_table(table, w, d, amp, max_pos,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_rope_apply(const void *x, void *y, int B, int H, int T, int d, int pos0,
+                          const float *table, int table_len, gqa_stream_t stream) {
+    if (!x || !y || !table || B <= 0 || H <= 0 || T <= 0 || table_len <= 0 || pos0 < 0)
+        return GQA_ERR_INVALID_ARG;
+    if (!rope_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(y) || !aligned16(table)) return GQA_ERR_ALIGNMENT;
+    if (static_cast<long>(pos0) + T > table_len) return GQA_ERR_RANGE;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    return from_cuda(gqa::launch_rope_apply(x, y, static_cast<long>(B) * H * T, T, d, pos0,
+                                            table, table_len, st,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t gqa_prefill_workspace_bytes(int B, int Hkv, int S, int d) {
+    if (B <= 0 || Hkv <= 0 || S <= 0 || d <= 0) return 0;
+    return static_cast<size_t>(B) * Hkv * S * d * 2;
+}
+
+gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int T, int S, int Hq, int Hkv, int d, int window,
+                            float scale, const float *table, int table_len, void *workspace,
+                            size_t workspace_bytes, gqa_stream_t stream) {
+    if (!q || !k || !v || !o || !table || B <= 0 || T <= 0 || S <= 0 || T > S || Hq <= 0 ||
+        Hkv <= 0 || (Hq % Hkv) != 0 || !std::isfinite(scale))
+        return GQA_ERR_INVALID_ARG;
+    if (d != 128) return GQA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(table) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return GQA_ERR_ALIGNMENT;
+    if (table_len < S) return GQA_ERR_RANGE;
+    const size_t need = gqa_prefill_workspace_bytes(B, Hkv, S, d);
+    if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GQA_ERR_ALIGNMENT;
+    // the grid is one CTA per (b, KV head, head pair, 128-row block)
+    const long blocks = static_cast<long>(B) * Hkv * ((Hq / Hkv + 1) / 2) * ((T + 127) / 128);
+    if (blocks > 0x7fffffffL) return GQA_ERR_UNSUPPORTED;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // K rotated once at positions 0..S-1 into the workspace; Q is rotated inside the
+    // attention kernel as each tile lands.
+    cudaError_t e = gqa::launch_rope_apply(k, workspace, static_cast<long>(B) * Hkv * S, S, d,
+                                           0, table, table_len, st, s);
+    if (e != cudaSuccess) return GQA_ERR_CUDA;
+    return static_cast<gqa_status>(gqa::launch_prefill(q, workspace, v, o, lse, B, T, S, Hq,
+                                                       Hkv, d, window, scale, table,
+                                                       table_len, st, s));
+}
+
+gqa_status gqa_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new, const void *v_new,
+                         int Hkv, int d, int32_t *slots_out, gqa_stream_t stream) {
+    if (!descs || !k_new || !v_new || nseq <= 0 || Hkv <= 0) return GQA_ERR_INVALID_ARG;
+    if (!rope_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
+    if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(descs) & 7u))
+        return GQA_ERR_ALIGNMENT;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    return from_cuda(gqa::launch_kv_append(descs, nseq, k_new, v_new, Hkv, d, slots_out, st,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t gqa_decode_workspace_bytes(int nseq, int Hq, int d, int max_len) {
+    if (nseq <= 0 || Hq <= 0 || d <= 0 || max_len <= 0) return 0;
+    const size_t ns = static_cast<size_t>(gqa::decode_num_splits(max_len));
+    return static_cast<size_t>(nseq) * Hq * ns * (d + 2) * sizeof(float);
+}
+
+gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
+                           int d, float scale, int max_len, void *o, float *lse,
+                           void *workspace, size_t workspace_bytes, gqa_stream_t stream) {
+    if (!q || !descs || !o || nseq <= 0 || Hq <= 0 || Hkv <= 0 || (Hq % Hkv) != 0 ||
+        max_len <= 0 || !std::isfinite(scale))
+        return GQA_ERR_INVALID_ARG;
+    if (d != 128 || Hq / Hkv > 8) return GQA_ERR_UNSUPPORTED;
+    if (nseq > 65535) return GQA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(o) || (reinterpret_cast<uintptr_t>(descs) & 7u) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return GQA_ERR_ALIGNMENT;
+    const size_t need = gqa_decode_workspace_bytes(nseq, Hq, d, max_len);
+    if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GQA_ERR_ALIGNMENT;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    return from_cuda(gqa::launch_decode(q, descs, nseq, Hq, Hkv, d, scale, max_len, o, lse,
+                                        static_cast<float *>(workspace), st,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_get_device_status(gqa_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, st, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(st, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return GQA_ERR_CUDA;
+    }
+    return static_cast<gqa_status>(v);
+}
+
+const char *gqa_status_string(int status) {
+    switch (status) {
+        case GQA_OK: return "ok";
+        case GQA_ERR_INVALID_ARG: return "invalid argument";
+        case GQA_ERR_UNSUPPORTED: return "unsupported shape or device";
+        case GQA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case GQA_ERR_CAPACITY: return "cache full or length beyond bound";
+        case GQA_ERR_CUDA: return "CUDA runtime error";
+        case GQA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case GQA_ERR_WORKSPACE: return "workspace missing or too small";
+        case GQA_ERR_RANGE: return "position beyond the RoPE table";
+        default: return "unknown status";
+    }
+}
+
+gqa_status gqa_device_check(void) {
+    int dev = 0;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    return (prop.major == 10 && prop.minor == 3) ? GQA_OK : GQA_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

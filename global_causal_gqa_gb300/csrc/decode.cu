@@ -1,0 +1,311 @@
+// decode.cu -- split-KV decode over a linear or ring KV cache, then an LSE combine.
+//
+// "PLaMo 3アーキテクチャ徹底解析": §4.4 (K cached before RoPE and rotated at every step,
+// keys at positions 0..R-1, query at R-1; the local ring keeps the newest W tokens),
+// §4.5 (attention equation), §2.3 (decode reads every cached K and V once per step:
+// 4 Hkv d bytes per token and layer -- the bound this kernel is written against).
+//
+// Work split: one CTA per (split of kDecodeChunk keys, sequence, block of <= 8 KV heads);
+// one warp per KV head streams its keys in blocks of 16 with 16-byte read-only loads.
+// The query group of G <= 8 heads shares every K and V element, so the per-block math
+// is two warp-level bf16 MMAs (m16n8k16): S^T = K' Q'^T and O^T += V^T P^T, fp32
+// accumulate.  The head dimension is permuted (identically on both operands of each
+// product) so that every 16-byte load lands directly in MMA fragment order and each
+// RoPE pair (j, j + 64) sits in one thread.  K is rotated in registers from the fp32
+// table at its logical position.  Each warp writes an unnormalised partial (m, l, O) for
+// its G heads; the combine kernel merges the splits by their log-sum-exp.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4 &u, int i) {
+    return i == 0 ? u.x : i == 1 ? u.y : i == 2 ? u.z : u.w;
+}
+
+// Rotates the 8 pairs (a[e], b[e]) held in two 16-byte chunks by the table entries
+// starting at `tab` (8 consecutive float2 = (amp cos, amp sin)).
+__device__ __forceinline__ void rotate8(uint4 &a, uint4 &b, const float2 *tab) {
+    const float4 *t4 = reinterpret_cast<const float4 *>(tab);
+    float cs[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 t = __ldg(t4 + q);
+        cs[4 * q] = t.x;
+        cs[4 * q + 1] = t.y;
+        cs[4 * q + 2] = t.z;
+        cs[4 * q + 3] = t.w;
+    }
+    uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float a0 = bf16lo(aw[q]), a1 = bf16hi(aw[q]);
+        const float b0 = bf16lo(bw[q]), b1 = bf16hi(bw[q]);
+        const float c0 = cs[4 * q], s0 = cs[4 * q + 1], c1 = cs[4 * q + 2], s1 = cs[4 * q + 3];
+        aw[q] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
+        bw[q] = pack_bf16x2(fmaf(a0, s0, b0 * c0), fmaf(a1, s1, b1 * c1));
+    }
+    a = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+    b = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+}
+
+struct SeqView {
+    int R;        // logical keys attended
+    int first;    // ring slot of logical key 0
+    int cap;
+    bool ok;
+};
+
+__device__ __forceinline__ SeqView seq_view(const gqa_kv_desc &desc, int max_len) {
+    SeqView v;
+    v.cap = desc.cap;
+    v.R = desc.is_ring ? min(desc.count, desc.cap) : desc.count;
+    v.first = desc.is_ring ? (desc.count - v.R) % max(desc.cap, 1) : 0;
+    v.ok = v.R > 0 && v.R <= max_len && v.R <= desc.rope_len && v.R <= desc.cap;
+    return v;
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+    decode_partial_kernel(const __nv_bfloat16 *__restrict__ q,
+                          const gqa_kv_desc *__restrict__ descs, int Hq, int Hkv,
+                          float scale_log2, int max_len, int nsplit, float *__restrict__ ws_ml,
+                          float *__restrict__ ws_o, int *status) {
+    const int split = blockIdx.x, seq = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = blockIdx.z * kWarps + warp;
+    const gqa_kv_desc desc = descs[seq];
+    const SeqView sv = seq_view(desc, max_len);
+    if (!sv.ok) {
+        if (split == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+            set_status(status, sv.R > max_len || sv.R > desc.cap ? GQA_ERR_CAPACITY
+                                                                   : GQA_ERR_RANGE);
+        return;
+    }
+    const int k_start = split * kDecodeChunk;
+    if (k_start >= sv.R || g >= Hkv) return;
+    const int k_end = min(sv.R, k_start + kDecodeChunk);
+    const int G = Hq / Hkv;
+    const int qpos = sv.R - 1;
+    const int gq = lane >> 2, tq = lane & 3;
+    const float2 *table = reinterpret_cast<const float2 *>(desc.rope);
+
+    // Q' as the B operand of S^T = K' Q'^T: thread (gq, tq) holds head gq, head-dim
+    // elements 32c + 8tq + e (c = 0..3, e = 0..7); k-chunk kc = 2c + (e >> 2).
+    uint32_t qb[8][2];
+    {
+        uint4 qc[4];
+        if (gq < G) {
+            const uint4 *qr = reinterpret_cast<const uint4 *>(
+                q + ((size_t)seq * Hq + (size_t)g * G + gq) * kD);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) qc[c] = qr[4 * c + tq];
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+                rotate8(qc[c], qc[c + 2], table + (size_t)qpos * (kD / 2) + 32 * c + 8 * tq);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) qc[c] = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            qb[2 * c][0] = qc[c].x;
+            qb[2 * c][1] = qc[c].y;
+            qb[2 * c + 1][0] = qc[c].z;
+            qb[2 * c + 1][1] = qc[c].w;
+        }
+    }
+
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m_run0 = -CUDART_INF_F, m_run1 = -CUDART_INF_F, l_run0 = 0.f, l_run1 = 0.f;
+
+    const __nv_bfloat16 *kbase = static_cast<const __nv_bfloat16 *>(desc.k) + (size_t)g * sv.cap * kD;
+    const __nv_bfloat16 *vbase = static_cast<const __nv_bfloat16 *>(desc.v) + (size_t)g * sv.cap * kD;
+    auto slot_of = [&](int key) {
+        int s = sv.first + key;
+        return s >= sv.cap ? s - sv.cap : s;
+    };
+
+    for (int kb = k_start; kb < k_end; kb += 16) {
+        // K rows kb + gq and kb + gq + 8; V rows kb + 2tq + {0, 1, 8, 9} (clamped in range;
+        // keys at or past k_end get weight 0).
+        const int key0 = kb + gq, key1 = kb + gq + 8;
+        const bool ok0 = key0 < k_end, ok1 = key1 < k_end;
+        const int kk0 = ok0 ? key0 : k_end - 1, kk1 = ok1 ? key1 : k_end - 1;
+        const uint4 *kr0 = reinterpret_cast<const uint4 *>(kbase + (size_t)slot_of(kk0) * kD);
+        const uint4 *kr1 = reinterpret_cast<const uint4 *>(kbase + (size_t)slot_of(kk1) * kD);
+        uint4 k0[4], k1[4], vv[4][2];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            k0[c] = ld_stream(kr0 + 4 * c + tq);
+            k1[c] = ld_stream(kr1 + 4 * c + tq);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            int key = kb + 2 * tq + (i & 1) + ((i >> 1) << 3);
+            key = key < k_end ? key : k_end - 1;
+            const uint4 *vr = reinterpret_cast<const uint4 *>(vbase + (size_t)slot_of(key) * kD);
+            vv[i][0] = ld_stream(vr + 2 * gq);
+            vv[i][1] = ld_stream(vr + 2 * gq + 1);
+        }
+        // rotate K at logical positions kk0, kk1
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            rotate8(k0[c], k0[c + 2], table + (size_t)kk0 * (kD / 2) + 32 * c + 8 * tq);
+            rotate8(k1[c], k1[c + 2], table + (size_t)kk1 * (kD / 2) + 32 * c + 8 * tq);
+        }
+        // S^T (16 keys x 8 heads)
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            mma16816(s, k0[c].x, k1[c].x, k0[c].y, k1[c].y, qb[2 * c][0], qb[2 * c][1]);
+            mma16816(s, k0[c].z, k1[c].z, k0[c].w, k1[c].w, qb[2 * c + 1][0], qb[2 * c + 1][1]);
+        }
+        // online softmax per head column (heads 2tq, 2tq+1), log2 domain
+        const float x0 = ok0 ? s[0] * scale_log2 : -CUDART_INF_F;
+        const float x1 = ok0 ? s[1] * scale_log2 : -CUDART_INF_F;
+        const float x2 = ok1 ? s[2] * scale_log2 : -CUDART_INF_F;
+        const float x3 = ok1 ? s[3] * scale_log2 : -CUDART_INF_F;
+        float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+        }
+        const float mn0 = fmaxf(m_run0, bm0), mn1 = fmaxf(m_run1, bm1);
+        const float f0 = ex2_approx(m_run0 - mn0), f1 = ex2_approx(m_run1 - mn1);
+        const float p0 = ex2_approx(x0 - mn0), p1 = ex2_approx(x1 - mn1);
+        const float p2 = ex2_approx(x2 - mn0), p3 = ex2_approx(x3 - mn1);
+        l_run0 = l_run0 * f0 + p0 + p2;
+        l_run1 = l_run1 * f1 + p1 + p3;
+        m_run0 = mn0;
+        m_run1 = mn1;
+        const uint32_t pb0 = transpose8x8(pack_bf16x2(p0, p1));
+        const uint32_t pb1 = transpose8x8(pack_bf16x2(p2, p3));
+        // O^T (128 dims x 8 heads) += V^T P^T; dims permuted: row g of m-tile mt is
+        // dim 16g + 2mt, row g + 8 is dim 16g + 2mt + 1.
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= f0;
+            o[mt][1] *= f1;
+            o[mt][2] *= f0;
+            o[mt][3] *= f1;
+            const uint32_t w0 = word(vv[0][mt >> 2], mt & 3), w1 = word(vv[1][mt >> 2], mt & 3);
+            const uint32_t w2 = word(vv[2][mt >> 2], mt & 3), w3 = word(vv[3][mt >> 2], mt & 3);
+            mma16816(o[mt], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
+                     __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), pb0, pb1);
+        }
+    }
+
+    // partial sums of l over the 8 key rows held across gq
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, off);
+        l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, off);
+    }
+    const int h0 = 2 * tq, h1 = 2 * tq + 1;  // heads within the group
+    const size_t rec0 = ((size_t)seq * Hq + (size_t)g * G + h0) * nsplit + split;
+    const size_t rec1 = ((size_t)seq * Hq + (size_t)g * G + h1) * nsplit + split;
+    if (h0 < G) {
+        if (gq == 0) {
+            ws_ml[2 * rec0] = m_run0;
+            ws_ml[2 * rec0 + 1] = l_run0;
+        }
+        float4 *dst = reinterpret_cast<float4 *>(ws_o + rec0 * kD + 16 * gq);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            dst[i] = make_float4(o[2 * i][0], o[2 * i][2], o[2 * i + 1][0], o[2 * i + 1][2]);
+    }
+    if (h1 < G) {
+        if (gq == 0) {
+            ws_ml[2 * rec1] = m_run1;
+            ws_ml[2 * rec1 + 1] = l_run1;
+        }
+        float4 *dst = reinterpret_cast<float4 *>(ws_o + rec1 * kD + 16 * gq);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            dst[i] = make_float4(o[2 * i][1], o[2 * i][3], o[2 * i + 1][1], o[2 * i + 1][3]);
+    }
+}
+
+// One block per (query head, sequence), one thread per head-dim element.
+__global__ void __launch_bounds__(kD)
+    decode_combine_kernel(const gqa_kv_desc *__restrict__ descs, int Hq, int max_len,
+                          int nsplit, const float *__restrict__ ws_ml,
+                          const float *__restrict__ ws_o, __nv_bfloat16 *__restrict__ out,
+                          float *__restrict__ lse) {
+    const int h = blockIdx.x, seq = blockIdx.y, dd = threadIdx.x;
+    const SeqView sv = seq_view(descs[seq], max_len);
+    if (!sv.ok) return;
+    const int ns = (sv.R + kDecodeChunk - 1) / kDecodeChunk;
+    const size_t rec = ((size_t)seq * Hq + h) * nsplit;
+    float M = -CUDART_INF_F;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, ws_ml[2 * (rec + s)]);
+    float L = 0.f, acc = 0.f;
+    for (int s = 0; s < ns; ++s) {
+        const float f = ex2_approx(ws_ml[2 * (rec + s)] - M);
+        L += ws_ml[2 * (rec + s) + 1] * f;
+        acc += ws_o[(rec + s) * kD + dd] * f;
+    }
+    out[((size_t)seq * Hq + h) * kD + dd] = __float2bfloat16_rn(acc / L);
+    if (lse && dd == 0) lse[(size_t)seq * Hq + h] = (M + __log2f(L)) * 0.69314718055994531f;
+}
+
+}  // namespace
+
+int decode_num_splits(int max_len) { return (max_len + kDecodeChunk - 1) / kDecodeChunk; }
+
+cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
+                          int d, float scale, int max_len, void *o, float *lse, float *ws,
+                          int *status, cudaStream_t s) {
+    (void)d;
+    const int nsplit = decode_num_splits(max_len);
+    float *ws_ml = ws;
+    float *ws_o = ws + (size_t)2 * nseq * Hq * nsplit;
+    const int warps = Hkv < kWarps ? Hkv : kWarps;
+    dim3 grid(nsplit, nseq, (Hkv + kWarps - 1) / kWarps);
+    const float scale_log2 = scale * 1.4426950408889634f;
+    decode_partial_kernel<<<grid, warps * 32, 0, s>>>(
+        static_cast<const __nv_bfloat16 *>(q), descs, Hq, Hkv, scale_log2, max_len, nsplit,
+        ws_ml, ws_o, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_combine_kernel<<<dim3(Hq, nseq), kD, 0, s>>>(descs, Hq, max_len, nsplit, ws_ml,
+                                                         ws_o, static_cast<__nv_bfloat16 *>(o),
+                                                         lse);
+    return cudaGetLastError();
+}
+
+}  // namespace gqa

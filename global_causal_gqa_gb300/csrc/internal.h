@@ -1,0 +1,39 @@
+// internal.h -- launchers shared between the kernel translation units and the C ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "gqa_attn.h"
+
+namespace gqa {
+
+constexpr int kMaxHeadDim = 512;
+
+struct InvFreq {
+    double w[kMaxHeadDim / 2];
+};
+
+// RoPE table and application (rope.cu)
+cudaError_t launch_rope_table(float *table, const InvFreq &w, int d, double amp, int max_pos,
+                              cudaStream_t s);
+cudaError_t launch_rope_apply(const void *x, void *y, long rows, int T, int d, int pos0,
+                              const float *table, int table_len, int *status, cudaStream_t s);
+
+// KV cache append (kv.cu)
+cudaError_t launch_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new,
+                             const void *v_new, int Hkv, int d, int32_t *slots,
+                             int *status, cudaStream_t s);
+
+// Decode (decode.cu)
+constexpr int kDecodeChunk = 1024;  // keys per split
+int decode_num_splits(int max_len);
+cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
+                          int d, float scale, int max_len, void *o, float *lse,
+                          float *ws, int *status, cudaStream_t s);
+
+// Prefill (prefill.cu); returns a gqa_status
+int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, float *lse,
+                   int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
+                   const float *table, int table_len, int *status, cudaStream_t s);
+
+}  // namespace gqa

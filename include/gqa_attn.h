@@ -1,0 +1,171 @@
+/*
+ * gqa_attn.h -- C ABI of the GB300 (sm_103a) causal grouped-query attention library.
+ *
+ * The library computes the attention of a hybrid local/global decoder layer:
+ *
+ *     O[b,h,t,:] = sum_s softmax_s( scale * <Q'[b,h,t,:], K'[b,g(h),s,:]> + M[t,s] ) V[b,g(h),s,:]
+ *
+ * with g(h) = floor(h / (Hq/Hkv)) (consecutive query heads share one KV head), Q' and K'
+ * the split-half RoPE rotations of Q and K, and M the causal or sliding-window mask.
+ * Definitions, by page and section:
+ *   "PLaMo 3アーキテクチャ徹底解析" (imoz.jp):
+ *     §4.2 grouped-query attention;  §4.4 the cache stores K before RoPE, positions are
+ *     generated inside attention (keys 0..S-1, queries S-T..S-1), the local cache keeps
+ *     the last W-1 tokens and re-numbers them;  §4.5 the attention equation, scale
+ *     1/sqrt(d), no softcap;  §5.1 the masks (causal j <= i; window also i - j < W,
+ *     self included);  §6.1 split-half RoPE, omega_j = theta^(-2j/d);  §6.3 YaRN
+ *     frequencies and the amplitude factor on cos and sin;  §6.4 partial (p-)RoPE.
+ *
+ * Conventions (all entry points):
+ *   - Tensors are bfloat16, dense, row-major in the layouts stated per call, in device
+ *     memory, 16-byte aligned.  The caller owns every buffer, descriptor array, workspace
+ *     and stream; the library allocates nothing and keeps no state except one device
+ *     status word per GPU.
+ *   - Every call validates its arguments on the host and returns a negative gqa_status
+ *     without launching anything if they are wrong.  Otherwise it enqueues its kernels on
+ *     `stream` (NULL = the legacy default stream) and returns GQA_OK without waiting.
+ *   - Errors found on the device (a bounded wait that expired, a full cache, an index
+ *     out of range) are recorded in the device status word and returned by the next
+ *     gqa_get_device_status().  Device code never traps.
+ *   - Head dims: prefill d in {128}; decode, kv_append and rope_apply d in {64, 128, 256,
+ *     512} (decode: d = 128).  Query group G = Hq/Hkv must be an integer; decode needs
+ *     G <= 16.  Other values return GQA_ERR_UNSUPPORTED.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *gqa_stream_t;
+
+typedef enum gqa_status {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARG = -1,     /* null pointer, non-positive size, inconsistent shape */
+    GQA_ERR_UNSUPPORTED = -2,     /* head dim / group size / device not supported */
+    GQA_ERR_ALIGNMENT = -3,       /* a pointer is not 16-byte aligned */
+    GQA_ERR_CAPACITY = -4,        /* a linear cache is full, or a length exceeds a bound */
+    GQA_ERR_CUDA = -5,            /* a CUDA runtime call failed */
+    GQA_ERR_DEVICE_TIMEOUT = -6,  /* a device-side bounded wait expired */
+    GQA_ERR_WORKSPACE = -7,       /* workspace missing or too small */
+    GQA_ERR_RANGE = -8            /* a position lies beyond the RoPE table */
+} gqa_status;
+
+/* ---- RoPE frequencies and table ---------------------------------------------------
+ * gqa_rope_inv_freq (host only, no GPU needed): writes omega_j, j = 0..d/2-1, to out:
+ *   omega_j = base^(-2j/d)                                        ("PLaMo 3..." §6.1)
+ *   if yarn_factor != 1 (YaRN, §6.3):
+ *     j_low  = (d/2) ln(yarn_L0 / (2 pi beta_fast)) / ln(base)   (not rounded)
+ *     j_high = (d/2) ln(yarn_L0 / (2 pi beta_slow)) / ln(base)
+ *     alpha_j = clip((j - j_low) / (j_high - j_low), 0, 1)
+ *     omega_j *= (1 - alpha_j) + alpha_j / yarn_factor
+ *   if rotate_fraction < 1 (p-RoPE, §6.4): omega_j = 0 for j >= round(rotate_fraction d/2);
+ *     the exponent keeps the full d.
+ * Returns GQA_ERR_INVALID_ARG for d odd/<= 0, base <= 1, yarn_factor < 1, or a fraction
+ * outside (0, 1]. */
+gqa_status gqa_rope_inv_freq(double *out, int d, double base, double yarn_factor,
+                             double yarn_L0, double beta_fast, double beta_slow,
+                             double rotate_fraction);
+
+/* YaRN amplitude 1 + 0.1 ln(s) applied to both cos and sin (§6.3); host only. */
+double gqa_yarn_amplitude(double s);
+
+/* Bytes of a RoPE table for head dim d and positions 0..max_pos-1:
+ * max_pos * (d/2) * 2 floats. */
+size_t gqa_rope_table_bytes(int d, int max_pos);
+
+/* Fills `table` (device, caller-owned, gqa_rope_table_bytes(d, max_pos) bytes) with
+ * float pairs table[p*(d/2) + j] = (amp cos(p omega_j), amp sin(p omega_j)) for
+ * p < max_pos: the angle and both functions are evaluated in double precision on the
+ * device and rounded once to float.  inv_freq: host array of d/2 doubles (see above),
+ * copied into the launch, so it may be freed on return.  d <= 512. */
+gqa_status gqa_rope_table_build(float *table, const double *inv_freq, int d, double amp,
+                                int max_pos, gqa_stream_t stream);
+
+/* ---- RoPE application (§6.1) --------------------------------------------------------
+ * y[b,h,t,:] = rotation of x[b,h,t,:] at position pos0 + t, pairs (j, j+d/2), using the
+ * table (table_len positions).  x, y: [B, H, T, d] bf16; y may equal x (in place).
+ * Each output is rounded once to bf16 from the float rotation. */
+gqa_status gqa_rope_apply(const void *x, void *y, int B, int H, int T, int d, int pos0,
+                          const float *table, int table_len, gqa_stream_t stream);
+
+/* ---- Prefill (§4.4, §4.5, §5.1) ------------------------------------------------------
+ * q: [B, Hq, T, d], k, v: [B, Hkv, S, d] (k before RoPE, as a cache holds it),
+ * o: [B, Hq, T, d] bf16.  lse: [B, Hq, T] float32 natural-log sum of exp of the scaled
+ * scores, or NULL.  T <= S; query t sits at position S - T + t, key s at position s.
+ * window <= 0: full causal; window > 0: keys with q_pos - k_pos < window (self included).
+ * scale multiplies the dot products (e.g. 1/sqrt(d)); the table's amplitude multiplies
+ * them by amp^2 on top.  table_len >= S.
+ * Key tiles wholly outside [q_pos - window + 1, q_pos] are never loaded or multiplied.
+ * workspace: device scratch of at least gqa_prefill_workspace_bytes(B, Hkv, S, d) bytes
+ * (it receives K rotated once); its contents are undefined afterwards.
+ * Supports d = 128.  Hq % Hkv == 0. */
+size_t gqa_prefill_workspace_bytes(int B, int Hkv, int S, int d);
+gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o,
+                            float *lse, int B, int T, int S, int Hq, int Hkv, int d,
+                            int window, float scale, const float *table, int table_len,
+                            void *workspace, size_t workspace_bytes, gqa_stream_t stream);
+
+/* ---- KV cache (§4.4) -----------------------------------------------------------------
+ * One descriptor per sequence, in device memory, owned by the caller.
+ *   k, v   : device [Hkv, cap, d] bf16, K stored before RoPE.
+ *   rope   : device RoPE table for this sequence's layer type; rope_len positions.
+ *   cap    : slots per KV head.
+ *   count  : linear cache (is_ring = 0): tokens held; they occupy slots 0..count-1 and
+ *            sit at positions equal to their slots.
+ *            ring cache (is_ring = 1, cap = window W): tokens appended so far; token i
+ *            lives in slot i mod cap.  Attention sees the newest min(count, cap) tokens,
+ *            re-numbered 0..R-1 from oldest to newest (the last W-1 kept plus the new one).
+ */
+typedef struct gqa_kv_desc {
+    void *k;
+    void *v;
+    const float *rope;
+    int32_t cap;
+    int32_t count;
+    int32_t is_ring;
+    int32_t rope_len;
+} gqa_kv_desc;
+
+/* Appends one token per sequence: k_new, v_new [nseq, Hkv, d] bf16 are written to slot
+ * count (linear) or count mod cap (ring) of every KV head, then count += 1.  slots_out
+ * (device int32[nseq], nullable) receives the slot written.  A full linear cache is not
+ * written; its slot_out is -1 and the status word records GQA_ERR_CAPACITY. */
+gqa_status gqa_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new,
+                         const void *v_new, int Hkv, int d, int32_t *slots_out,
+                         gqa_stream_t stream);
+
+/* ---- Decode (§4.4, §4.5) ---------------------------------------------------------------
+ * One query token per sequence: q [nseq, Hq, d] bf16 at position R-1, where R = count
+ * (linear) or min(count, cap) (ring) read from the descriptors (so call after
+ * gqa_kv_append).  Keys are the R logical tokens at positions 0..R-1, rotated on the fly
+ * with the sequence's table.  o: [nseq, Hq, d] bf16; lse: [nseq, Hq] float or NULL.
+ * max_len: an upper bound on R over the batch (sizes the split-KV grid); a sequence with
+ * R > max_len or rope_len < R is skipped and flagged in the status word.
+ * workspace: device scratch of gqa_decode_workspace_bytes(nseq, Hq, d, max_len) bytes.
+ * d = 128, Hq/Hkv <= 16. */
+size_t gqa_decode_workspace_bytes(int nseq, int Hq, int d, int max_len);
+gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq,
+                           int Hkv, int d, float scale, int max_len, void *o, float *lse,
+                           void *workspace, size_t workspace_bytes, gqa_stream_t stream);
+
+/* ---- Status ----------------------------------------------------------------------------
+ * Waits for `stream`, then returns and clears the current device's status word
+ * (GQA_OK if no device-side error was recorded since the last call). */
+gqa_status gqa_get_device_status(gqa_stream_t stream);
+
+/* Static, human-readable text for a status code. */
+const char *gqa_status_string(int status);
+
+/* GQA_OK if the current CUDA device is an sm_103 part this build can run on. */
+gqa_status gqa_device_check(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GQA_ATTN_H */

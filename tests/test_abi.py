@@ -1,0 +1,79 @@
+"""The C-ABI library without a GPU: it loads, exports every function the header declares,
+its host-only functions agree with the oracle, and bad arguments are rejected on the
+host before anything is launched."""
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import global_causal_gqa_gb300 as gqa
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "gqa_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = gqa.lib()
+    names = _declared()
+    assert len(names) >= 13, names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_inv_freq_matches_oracle():
+    orc = oracle.default()
+    for args in [(128, 1e4), (128, 1e6, 8.0), (128, 1e6, 256.0), (512, 1e6, 1.0, 4096, 32, 1, 0.25),
+                 (256, 1e4), (64, 5e5, 4.0, 8192, 16, 2)]:
+        a = gqa.gqa_rope_inv_freq(*args)
+        b = orc.inv_freq(*args)
+        assert np.max(np.abs(a - b)) <= 1e-15 * np.max(np.abs(b)), args
+
+
+def test_yarn_amplitude_and_sizes():
+    assert abs(gqa.gqa_yarn_amplitude(256.0) - (1 + 0.1 * math.log(256))) < 1e-15
+    assert gqa.gqa_rope_table_bytes(128, 1000) == 1000 * 64 * 2 * 4
+    assert gqa.gqa_prefill_workspace_bytes(2, 8, 8192, 128) == 2 * 8 * 8192 * 128 * 2
+    assert gqa.gqa_decode_workspace_bytes(32, 64, 128, 65536) == 32 * 64 * 64 * 130 * 4
+    assert gqa.gqa_rope_table_bytes(0, 10) == 0
+
+
+def test_bad_arguments_rejected_on_host():
+    L = gqa.lib()
+    S = gqa.STATUS_NAMES
+    f = lambda st: S.get(st, st)  # noqa: E731
+    with pytest.raises(gqa.GQAError):
+        gqa.gqa_rope_inv_freq(127, 1e4)
+    # null pointers
+    assert f(L.gqa_attn_prefill(None, None, None, None, None, 1, 8, 8, 2, 1, 128, 0, 0.1,
+                                None, 8, None, 0, None)) == "GQA_ERR_INVALID_ARG"
+    fake = 0x10000
+    # T > S, Hq not a multiple of Hkv
+    assert f(L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 9, 8, 2, 1, 128, 0, 0.1, fake,
+                                8, fake, 1 << 20, None)) == "GQA_ERR_INVALID_ARG"
+    assert f(L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 3, 2, 128, 0, 0.1, fake,
+                                8, fake, 1 << 20, None)) == "GQA_ERR_INVALID_ARG"
+    # unsupported head dim, misaligned pointer, short table, small workspace
+    assert f(L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 2, 1, 96, 0, 0.1, fake,
+                                8, fake, 1 << 20, None)) == "GQA_ERR_UNSUPPORTED"
+    assert f(L.gqa_attn_prefill(fake + 8, fake, fake, fake, None, 1, 8, 8, 2, 1, 128, 0, 0.1,
+                                fake, 8, fake, 1 << 20, None)) == "GQA_ERR_ALIGNMENT"
+    assert f(L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 2, 1, 128, 0, 0.1, fake,
+                                7, fake, 1 << 20, None)) == "GQA_ERR_RANGE"
+    assert f(L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 2, 1, 128, 0, 0.1, fake,
+                                8, fake, 10, None)) == "GQA_ERR_WORKSPACE"
+    # decode: group larger than supported, small workspace
+    assert f(L.gqa_attn_decode(fake, fake, 1, 32, 2, 128, 0.1, 64, fake, None, fake, 1 << 20,
+                               None)) == "GQA_ERR_UNSUPPORTED"
+    assert f(L.gqa_attn_decode(fake, fake, 1, 8, 1, 128, 0.1, 64, fake, None, fake, 8,
+                               None)) == "GQA_ERR_WORKSPACE"
+    assert f(L.gqa_kv_append(None, 1, fake, fake, 1, 128, None, None)) == "GQA_ERR_INVALID_ARG"
+    assert f(L.gqa_rope_apply(fake, fake, 1, 1, 4, 128, 10, fake, 12, None)) == "GQA_ERR_RANGE"
+    assert gqa.gqa_status_string(-6) == "device-side wait timed out"

@@ -1,0 +1,118 @@
+"""Prefill parity: gqa_attn_prefill (C-ABI, tcgen05 kernel) against the fp64 oracle.
+
+Small cases compare every output element; the full-size PLaMo-3-shaped workloads
+(same launch configuration the benchmark times) compare a seeded sample of rows that
+always includes the window edges, tile edges and the last row.  Bar: max abs 2e-2 and
+mean abs 2e-3 on the bf16 outputs; lse within 2e-2.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_utils as gu
+from workloads import WORKLOADS, PrefillLayer, RopeSpec, prefill_inputs
+
+pytestmark = pytest.mark.gpu
+
+LOCAL = RopeSpec(base=1e4)
+YARN = RopeSpec(base=1e6, yarn_factor=8.0, amp=math.sqrt(1.2))
+
+
+def _full_case(layer: PrefillLayer):
+    gu.require_gpu()
+    x = prefill_inputs(layer)
+    q, k, v = gu.to_cuda(x.q, x.k, x.v)
+    table = gu.rope_table(layer.d, layer.rope, layer.S)
+    o, lse = gu.run_prefill(q, k, v, layer.window, layer.scale, table, layer.S)
+    w = gu.oracle_freq(layer.d, layer.rope)
+    ro, rl = gu.orc().attention(x.q, x.k, x.v, window=layer.window, scale=layer.scale, w=w,
+                                amp=layer.rope.amp)
+    gu.compare(o, ro, what=layer.label)
+    gu.compare(lse, rl, max_abs=2e-2, mean_abs=2e-3, what=layer.label + " lse")
+    return o
+
+
+@pytest.mark.parametrize("name", ["tiny_w64", "tiny_causal"])
+def test_tiny_workloads(name):
+    _full_case(WORKLOADS[name].layers[0])
+
+
+def _layer(B, T, S, Hq, Hkv, W, rope=LOCAL, seed=7, d=128):
+    return PrefillLayer(B=B, T=T, S=S, Hq=Hq, Hkv=Hkv, d=d, window=W, rope=rope,
+                        scale=1 / math.sqrt(d), seed=seed)
+
+
+EDGE_CASES = [
+    # ragged tails, several tiles, tiny windows, windows at tile edges
+    _layer(1, 200, 200, 2, 1, 0, seed=11),
+    _layer(1, 1, 1, 2, 1, 0, seed=12),
+    _layer(1, 130, 130, 4, 2, 1, seed=13),
+    _layer(1, 300, 300, 4, 1, 4, seed=14),
+    _layer(1, 384, 384, 2, 1, 127, seed=15),
+    _layer(1, 384, 384, 2, 1, 128, seed=16),
+    _layer(1, 384, 384, 2, 1, 129, seed=17),
+    _layer(2, 257, 257, 6, 2, 64, YARN, seed=18),
+    # odd group (last head pair has one head), MHA, MQA
+    _layer(1, 160, 160, 3, 1, 0, seed=19),
+    _layer(1, 160, 160, 2, 2, 50, seed=20),
+    _layer(1, 256, 256, 8, 1, 0, YARN, seed=21),
+    # queries at the end of a longer key range (chunked prefill: q_pos = S - T + t)
+    _layer(1, 100, 300, 4, 2, 0, seed=22),
+    _layer(1, 129, 700, 4, 2, 200, YARN, seed=23),
+    _layer(1, 1, 513, 2, 1, 0, seed=24),
+]
+
+
+@pytest.mark.parametrize("layer", EDGE_CASES, ids=lambda l: l.label)
+def test_edge_cases(layer):
+    _full_case(layer)
+
+
+def test_window_at_least_T_equals_causal():
+    """A window as wide as the sequence removes nothing: bit-identical to full causal."""
+    gu.require_gpu()
+    a = _full_case(_layer(1, 320, 320, 4, 2, 0, seed=31))
+    b = _full_case(_layer(1, 320, 320, 4, 2, 320, seed=31))
+    c = _full_case(_layer(1, 320, 320, 4, 2, 100000, seed=31))
+    assert torch.equal(a, b) and torch.equal(a, c)
+
+
+def test_deterministic():
+    gu.require_gpu()
+    a = _full_case(_layer(1, 256, 256, 4, 1, 70, seed=41))
+    b = _full_case(_layer(1, 256, 256, 4, 1, 70, seed=41))
+    assert torch.equal(a, b)
+
+
+def _sampled_case(layer: PrefillLayer, n_rows: int, seed: int):
+    gu.require_gpu()
+    x = prefill_inputs(layer)
+    q, k, v = gu.to_cuda(x.q, x.k, x.v)
+    table = gu.rope_table(layer.d, layer.rope, layer.S)
+    o, lse = gu.run_prefill(q, k, v, layer.window, layer.scale, table, layer.S)
+    rows = gu.sample_rows(layer.B, layer.Hq, layer.Hkv, layer.T, layer.window, n_rows, seed)
+    w = gu.oracle_freq(layer.d, layer.rope)
+    ro, rl = gu.orc().attention(x.q, x.k, x.v, window=layer.window, scale=layer.scale, w=w,
+                                amp=layer.rope.amp, rows=rows)
+    idx = torch.from_numpy(rows.astype(np.int64))
+    og = o.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]]
+    lg = lse.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]]
+    gu.compare(og, ro, what=layer.label + " sampled")
+    gu.compare(lg, rl, what=layer.label + " sampled lse")
+    assert torch.isfinite(o).all()
+
+
+def test_medium_window_sampled():
+    _sampled_case(_layer(1, 4096, 4096, 16, 2, 2048, seed=51), 1024, 1)
+
+
+def test_plamo3_local_prefill_full_size_sampled():
+    """B=2, T=S=8192, 64/8 heads, d=128, W=2048 -- the benchmark's launch."""
+    _sampled_case(WORKLOADS["plamo3_local_prefill"].layers[0], 4096, 2)
+
+
+def test_plamo3_global_prefill_full_size_sampled():
+    """B=1, T=S=32768, 64/8 heads, YaRN (s=8), logits x1.2, full causal."""
+    _sampled_case(WORKLOADS["plamo3_global_prefill"].layers[0], 4096, 3)
