@@ -71,7 +71,7 @@ def lib() -> ctypes.CDLL:
             "gqa_rope_table_build": ([P, P, I, D, I, P], I),
             "gqa_rope_apply": ([P, P, I, I, I, I, I, P, I, P], I),
             "gqa_prefill_workspace_bytes": ([I, I, I, I], Z),
-            "gqa_attn_prefill": ([P, P, P, P, P, I, I, I, I, I, I, I, F, P, I, P, Z, P], I),
+            "gqa_attn_prefill": ([P, P, P, P, P, I, I, I, I, I, I, I, F, P, I, I, P, Z, P], I),
             "gqa_kv_append": ([P, I, P, P, I, I, P, P], I),
             "gqa_decode_workspace_bytes": ([I, I, I, I], Z),
             "gqa_attn_decode": ([P, P, I, I, I, I, F, I, P, P, P, Z, P], I),
@@ -155,11 +155,11 @@ def gqa_prefill_workspace_bytes(B: int, Hkv: int, S: int, d: int) -> int:
 
 
 def gqa_attn_prefill(q, k, v, o, lse, B: int, T: int, S: int, Hq: int, Hkv: int, d: int,
-                     window: int, scale: float, table, table_len: int, workspace,
-                     workspace_bytes: int, stream=None, check: bool = True) -> int:
+                     window: int, scale: float, table, table_len: int, k_is_rotated: int,
+                     workspace, workspace_bytes: int, stream=None, check: bool = True) -> int:
     st = lib().gqa_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, S, Hq,
-                                Hkv, d, window, scale, _ptr(table), table_len, _ptr(workspace),
-                                workspace_bytes, _stream(stream))
+                                Hkv, d, window, scale, _ptr(table), table_len, k_is_rotated,
+                                _ptr(workspace), workspace_bytes, _stream(stream))
     return _check("gqa_attn_prefill", st, check)
 
 

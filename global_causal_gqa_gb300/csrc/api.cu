@@ -114,8 +114,8 @@ size_t gqa_prefill_workspace_bytes(int B, int Hkv, int S, int d) {
 
 gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o, float *lse,
                             int B, int T, int S, int Hq, int Hkv, int d, int window,
-                            float scale, const float *table, int table_len, void *workspace,
-                            size_t workspace_bytes, gqa_stream_t stream) {
+                            float scale, const float *table, int table_len, int k_is_rotated,
+                            void *workspace, size_t workspace_bytes, gqa_stream_t stream) {
     if (!q || !k || !v || !o || !table || B <= 0 || T <= 0 || S <= 0 || T > S || Hq <= 0 ||
         Hkv <= 0 || (Hq % Hkv) != 0 || !std::isfinite(scale))
         return GQA_ERR_INVALID_ARG;
@@ -124,9 +124,11 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
         (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return GQA_ERR_ALIGNMENT;
     if (table_len < S) return GQA_ERR_RANGE;
-    const size_t need = gqa_prefill_workspace_bytes(B, Hkv, S, d);
-    if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return GQA_ERR_ALIGNMENT;
+    if (!k_is_rotated) {
+        const size_t need = gqa_prefill_workspace_bytes(B, Hkv, S, d);
+        if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return GQA_ERR_ALIGNMENT;
+    }
     // the grid is one CTA per (b, KV head, head pair, 128-row block)
     const long blocks = static_cast<long>(B) * Hkv * ((Hq / Hkv + 1) / 2) * ((T + 127) / 128);
     if (blocks > 0x7fffffffL) return GQA_ERR_UNSUPPORTED;
@@ -135,10 +137,14 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // K rotated once at positions 0..S-1 into the workspace; Q is rotated inside the
     // attention kernel as each tile lands.
-    cudaError_t e = gqa::launch_rope_apply(k, workspace, static_cast<long>(B) * Hkv * S, S, d,
-                                           0, table, table_len, st, s);
-    if (e != cudaSuccess) return GQA_ERR_CUDA;
-    return static_cast<gqa_status>(gqa::launch_prefill(q, workspace, v, o, lse, B, T, S, Hq,
+    const void *k_rot = k;
+    if (!k_is_rotated) {
+        cudaError_t e = gqa::launch_rope_apply(k, workspace, static_cast<long>(B) * Hkv * S, S,
+                                               d, 0, table, table_len, st, s);
+        if (e != cudaSuccess) return GQA_ERR_CUDA;
+        k_rot = workspace;
+    }
+    return static_cast<gqa_status>(gqa::launch_prefill(q, k_rot, v, o, lse, B, T, S, Hq,
                                                        Hkv, d, window, scale, table,
                                                        table_len, st, s));
 }

@@ -102,14 +102,18 @@ gqa_status gqa_rope_apply(const void *x, void *y, int B, int H, int T, int d, in
  * scale multiplies the dot products (e.g. 1/sqrt(d)); the table's amplitude multiplies
  * them by amp^2 on top.  table_len >= S.
  * Key tiles wholly outside [q_pos - window + 1, q_pos] are never loaded or multiplied.
- * workspace: device scratch of at least gqa_prefill_workspace_bytes(B, Hkv, S, d) bytes
- * (it receives K rotated once); its contents are undefined afterwards.
+ * k_is_rotated = 0: k holds keys before RoPE (as the PLaMo cache stores them, §4.4); they
+ *   are rotated once at positions 0..S-1 into `workspace`, which must hold at least
+ *   gqa_prefill_workspace_bytes(B, Hkv, S, d) bytes; its contents are undefined afterwards.
+ * k_is_rotated = 1: k already carries RoPE (a cache that stores rotated keys, as Gemma's
+ *   does, §4.4); workspace may be NULL.
  * Supports d = 128.  Hq % Hkv == 0. */
 size_t gqa_prefill_workspace_bytes(int B, int Hkv, int S, int d);
 gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o,
                             float *lse, int B, int T, int S, int Hq, int Hkv, int d,
                             int window, float scale, const float *table, int table_len,
-                            void *workspace, size_t workspace_bytes, gqa_stream_t stream);
+                            int k_is_rotated, void *workspace, size_t workspace_bytes,
+                            gqa_stream_t stream);
 
 /* ---- KV cache (§4.4) -----------------------------------------------------------------
  * One descriptor per sequence, in device memory, owned by the caller.

@@ -53,7 +53,7 @@ def run_prefill(q, k, v, window: int, scale: float, table: torch.Tensor, table_l
     wsb = gqa.gqa_prefill_workspace_bytes(B, Hkv, S, d)
     ws = torch.empty(wsb, dtype=torch.uint8, device=q.device)
     gqa.gqa_attn_prefill(q, k, v, o, lse, B, T, S, Hq, Hkv, d, window, scale, table,
-                         table_len, ws, wsb)
+                         table_len, 0, ws, wsb)
     st = gqa.gqa_get_device_status()
     assert st == 0, f"device status {gqa.STATUS_NAMES.get(st, st)}"
     return o, lse

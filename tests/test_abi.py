@@ -53,22 +53,22 @@ def test_bad_arguments_rejected_on_host():
         gqa.gqa_rope_inv_freq(127, 1e4)
     # null pointers
     assert f(L.gqa_attn_prefill(None, None, None, None, None, 1, 8, 8, 2, 1, 128, 0, 0.1,
-                                None, 8, None, 0, None)) == "GQA_ERR_INVALID_ARG"
+                                None, 8, 0, None, 0, None)) == "GQA_ERR_INVALID_ARG"
     fake = 0x10000
     # T > S, Hq not a multiple of Hkv
     assert f(L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 9, 8, 2, 1, 128, 0, 0.1, fake,
-                                8, fake, 1 << 20, None)) == "GQA_ERR_INVALID_ARG"
+                                8, 0, fake, 1 << 20, None)) == "GQA_ERR_INVALID_ARG"
     assert f(L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 3, 2, 128, 0, 0.1, fake,
-                                8, fake, 1 << 20, None)) == "GQA_ERR_INVALID_ARG"
+                                8, 0, fake, 1 << 20, None)) == "GQA_ERR_INVALID_ARG"
     # unsupported head dim, misaligned pointer, short table, small workspace
     assert f(L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 2, 1, 96, 0, 0.1, fake,
-                                8, fake, 1 << 20, None)) == "GQA_ERR_UNSUPPORTED"
+                                8, 0, fake, 1 << 20, None)) == "GQA_ERR_UNSUPPORTED"
     assert f(L.gqa_attn_prefill(fake + 8, fake, fake, fake, None, 1, 8, 8, 2, 1, 128, 0, 0.1,
-                                fake, 8, fake, 1 << 20, None)) == "GQA_ERR_ALIGNMENT"
+                                fake, 8, 0, fake, 1 << 20, None)) == "GQA_ERR_ALIGNMENT"
     assert f(L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 2, 1, 128, 0, 0.1, fake,
-                                7, fake, 1 << 20, None)) == "GQA_ERR_RANGE"
+                                7, 0, fake, 1 << 20, None)) == "GQA_ERR_RANGE"
     assert f(L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 2, 1, 128, 0, 0.1, fake,
-                                8, fake, 10, None)) == "GQA_ERR_WORKSPACE"
+                                8, 0, fake, 10, None)) == "GQA_ERR_WORKSPACE"
     # decode: group larger than supported, small workspace
     assert f(L.gqa_attn_decode(fake, fake, 1, 32, 2, 128, 0.1, 64, fake, None, fake, 1 << 20,
                                None)) == "GQA_ERR_UNSUPPORTED"
