@@ -23,7 +23,8 @@ __all__ = [
     "GQAError", "lib", "KV_DESC_DTYPE", "make_kv_descs",
     "gqa_rope_inv_freq", "gqa_yarn_amplitude", "gqa_rope_table_bytes", "gqa_rope_table_build",
     "gqa_rope_apply", "gqa_prefill_workspace_bytes", "gqa_attn_prefill", "gqa_kv_append",
-    "gqa_decode_workspace_bytes", "gqa_attn_decode", "gqa_get_device_status",
+    "gqa_decode_workspace_bytes", "gqa_attn_decode", "gqa_attn_decode_static",
+    "gqa_get_device_status",
     "gqa_status_string", "gqa_device_check",
 ]
 
@@ -75,6 +76,7 @@ def lib() -> ctypes.CDLL:
             "gqa_kv_append": ([P, I, P, P, I, I, P, P], I),
             "gqa_decode_workspace_bytes": ([I, I, I, I], Z),
             "gqa_attn_decode": ([P, P, I, I, I, I, F, I, P, P, P, Z, P], I),
+            "gqa_attn_decode_static": ([P, P, I, I, I, I, F, I, P, P, P], I),
             "gqa_get_device_status": ([P], I),
             "gqa_status_string": ([I], ctypes.c_char_p),
             "gqa_device_check": ([], I),
@@ -195,6 +197,16 @@ def gqa_attn_decode(q, descs, nseq: int, Hq: int, Hkv: int, d: int, scale: float
     st = lib().gqa_attn_decode(_ptr(q), _ptr(descs), nseq, Hq, Hkv, d, scale, max_len, _ptr(o),
                                _ptr(lse), _ptr(workspace), workspace_bytes, _stream(stream))
     return _check("gqa_attn_decode", st, check)
+
+
+def gqa_attn_decode_static(q, descs, nseq: int, Hq: int, Hkv: int, d: int, scale: float,
+                           max_len: int, o, lse, stream=None, check: bool = True) -> int:
+    """gqa_attn_decode without a workspace argument: for callers that cannot allocate
+    device memory; the partials use a fixed 16 MiB array inside the library (shared by all
+    calls, so overlapping calls race)."""
+    st = lib().gqa_attn_decode_static(_ptr(q), _ptr(descs), nseq, Hq, Hkv, d, scale, max_len,
+                                      _ptr(o), _ptr(lse), _stream(stream))
+    return _check("gqa_attn_decode_static", st, check)
 
 
 # ---- status ---------------------------------------------------------------------------------

@@ -188,6 +188,57 @@ gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, in
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// ---- decode with library-owned scratch (no allocation) ---------------------------------
+// Some callers cannot hand the library a workspace: their device memory belongs to another
+// component (a framework allocator that has reserved the GPU's memory up front, a serving
+// runtime that forbids allocating inside its step loop), or they cannot afford the device
+// synchronisation that cudaMalloc/cudaFree imply on every decode step.  For them the
+// split-KV partials of one decode call live in this fixed array, compiled into the library
+// and present on every GPU that loads it until the process exits.
+constexpr size_t kDecodeStaticScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_decode_static_scratch[kDecodeStaticScratchBytes];
+
+// Device address of the array on the current device.  In host code the array's name only
+// stands in for the symbol; a kernel must be given this address instead.  Looked up once
+// per device, with that device current, on the first call made on it.
+static float *decode_static_scratch(void) {
+    static std::mutex mu;
+    static float *ptrs[kMaxDevices] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_static_scratch) != cudaSuccess || !p) return nullptr;
+        ptrs[dev] = static_cast<float *>(p);
+    }
+    return ptrs[dev];
+}
+
+gqa_status gqa_attn_decode_static(const void *q, const gqa_kv_desc *descs, int nseq, int Hq,
+                                  int Hkv, int d, float scale, int max_len, void *o,
+                                  float *lse, gqa_stream_t stream) {
+    if (!q || !descs || !o || nseq <= 0 || Hq <= 0 || Hkv <= 0 || (Hq % Hkv) != 0 ||
+        max_len <= 0 || !std::isfinite(scale))
+        return GQA_ERR_INVALID_ARG;
+    if (d != 128 || Hq / Hkv > 8) return GQA_ERR_UNSUPPORTED;
+    if (nseq > 65535) return GQA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(o) || (reinterpret_cast<uintptr_t>(descs) & 7u) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return GQA_ERR_ALIGNMENT;
+    // the partials of this call must fit the fixed array
+    if (gqa_decode_workspace_bytes(nseq, Hq, d, max_len) > kDecodeStaticScratchBytes)
+        return GQA_ERR_WORKSPACE;
+    float *scratch = decode_static_scratch();
+    if (!scratch) return GQA_ERR_CUDA;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    // Every partial record the combine pass reads is written earlier in the same call, so
+    // nothing left in the array by a previous call is ever read: no clearing is needed.
+    return from_cuda(gqa::launch_decode(q, descs, nseq, Hq, Hkv, d, scale, max_len, o, lse,
+                                        scratch, st, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 gqa_status gqa_get_device_status(gqa_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return GQA_ERR_CUDA;

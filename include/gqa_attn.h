@@ -158,6 +158,26 @@ gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, in
                            int Hkv, int d, float scale, int max_len, void *o, float *lse,
                            void *workspace, size_t workspace_bytes, gqa_stream_t stream);
 
+/* Decode without a caller-supplied workspace; allocates nothing.  The pages have no
+ * counterpart to this entry point: it is the same computation as gqa_attn_decode (same
+ * kernels, same arguments and results), for callers that cannot provide scratch memory --
+ * for instance because their device memory is owned by another component (a framework
+ * allocator that reserved the GPU up front, a serving loop that forbids allocation), or
+ * because the device synchronisation of cudaMalloc/cudaFree is unacceptable per step.
+ * The split-KV partials go to a fixed 16 MiB device array inside the library, which every
+ * GPU that loads the library holds until the process exits.  A call whose partials need
+ * more than that, i.e. gqa_decode_workspace_bytes(nseq, Hq, d, max_len) > 16 MiB, returns
+ * GQA_ERR_WORKSPACE without launching.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.
+ * All calls share the one array and it keeps the last call's contents (each call writes
+ * every record it reads, so no clearing is needed): calls that may overlap on the GPU --
+ * on different streams, or from different host threads -- race on it and must be
+ * serialised by the caller. */
+gqa_status gqa_attn_decode_static(const void *q, const gqa_kv_desc *descs, int nseq, int Hq,
+                                  int Hkv, int d, float scale, int max_len, void *o,
+                                  float *lse, gqa_stream_t stream);
+
 /* ---- Status ----------------------------------------------------------------------------
  * Waits for `stream`, then returns and clears the current device's status word
  * (GQA_OK if no device-side error was recorded since the last call). */
