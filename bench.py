@@ -165,6 +165,16 @@ class Timer:
         return [[a.elapsed_time(b) for a, b in zip(ev[:-1], ev[1:])] for ev in self.records]
 
 
+def load_phase(timer, step, seconds: float = 1.0):
+    """Untimed steps for about `seconds` right before the timed region, so the clock
+    sampler (one sample per 200 ms) sees the GPU under this load; the reported clocks
+    cover this phase and the timed steps."""
+    t_end = time.perf_counter() + seconds
+    while time.perf_counter() < t_end:
+        timer.run(1, step, timed=False)
+        timer.torch.cuda.synchronize()
+
+
 def dist_setup(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -240,6 +250,7 @@ def bench_prefill(layer, steps: int, warmup: int, stream, peaks, peak_src, world
     sampler = ClockSampler(clocks_index) if clocks_index is not None else None
     if sampler:
         sampler.__enter__()
+        load_phase(timer, step)
     t0 = time.perf_counter()
     timer.run(steps, step)
     torch.cuda.synchronize()
@@ -362,6 +373,7 @@ def bench_decode(w, steps, warmup, stream, peaks, peak_src, world, with_e2e, clo
     sampler = ClockSampler(clocks_index) if clocks_index is not None else None
     if sampler:
         sampler.__enter__()
+        load_phase(timer, step)
     timer.run(steps, step)
     torch.cuda.synchronize()
     barrier(world)

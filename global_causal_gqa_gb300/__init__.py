@@ -25,7 +25,7 @@ __all__ = [
     "gqa_rope_apply", "gqa_prefill_workspace_bytes", "gqa_attn_prefill", "gqa_kv_append",
     "gqa_decode_workspace_bytes", "gqa_attn_decode", "gqa_attn_decode_static",
     "gqa_get_device_status",
-    "gqa_status_string", "gqa_device_check",
+    "gqa_status_string", "gqa_last_error_string", "gqa_device_check",
 ]
 
 GQA_OK = 0
@@ -39,8 +39,10 @@ STATUS_NAMES = {
 class GQAError(RuntimeError):
     def __init__(self, func: str, status: int):
         self.status = status
-        super().__init__(f"{func}: {STATUS_NAMES.get(status, status)} "
-                         f"({gqa_status_string(status)})")
+        detail = gqa_status_string(status)
+        if status == -5:
+            detail += ": " + gqa_last_error_string()
+        super().__init__(f"{func}: {STATUS_NAMES.get(status, status)} ({detail})")
 
 
 # struct gqa_kv_desc { void *k; void *v; const float *rope; int32 cap, count, is_ring, rope_len; }
@@ -79,6 +81,7 @@ def lib() -> ctypes.CDLL:
             "gqa_attn_decode_static": ([P, P, I, I, I, I, F, I, P, P, P], I),
             "gqa_get_device_status": ([P], I),
             "gqa_status_string": ([I], ctypes.c_char_p),
+            "gqa_last_error_string": ([], ctypes.c_char_p),
             "gqa_device_check": ([], I),
         }
         for name, (args, res) in sig.items():
@@ -217,6 +220,10 @@ def gqa_get_device_status(stream=None) -> int:
 
 def gqa_status_string(status: int) -> str:
     return lib().gqa_status_string(status).decode()
+
+
+def gqa_last_error_string() -> str:
+    return lib().gqa_last_error_string().decode()
 
 
 def gqa_device_check() -> int:

@@ -3,6 +3,7 @@
 Each translation unit is compiled in parallel with `-gencode arch=compute_103a,
 code=sm_103a -lineinfo -O3`, then linked with `nvcc -shared` (static CUDA runtime, so
 the library loads on a machine without a GPU and needs no libcuda at link time).
+Extra nvcc flags may be given in the GQA_NVCC_FLAGS environment variable.
 """
 from __future__ import annotations
 
@@ -51,7 +52,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, *ARCH, *FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        env_flags = os.environ.get("GQA_NVCC_FLAGS", "").split()
+        cmd = [cc, *ARCH, *FLAGS, *extra_flags, *env_flags, "-c", os.path.join(CSRC, src),
+               "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)

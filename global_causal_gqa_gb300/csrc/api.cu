@@ -38,7 +38,14 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool rope_dim_ok(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
 
-gqa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA; }
+// The CUDA error behind the most recent GQA_ERR_CUDA returned on this host thread.
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+gqa_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return GQA_OK;
+    t_last_cuda_error = e;
+    return GQA_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -144,9 +151,10 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
         if (e != cudaSuccess) return GQA_ERR_CUDA;
         k_rot = workspace;
     }
-    return static_cast<gqa_status>(gqa::launch_prefill(q, k_rot, v, o, lse, B, T, S, Hq,
-                                                       Hkv, d, window, scale, table,
-                                                       table_len, st, s));
+    const int rc = gqa::launch_prefill(q, k_rot, v, o, lse, B, T, S, Hq, Hkv, d, window, scale,
+                                       table, table_len, st, s);
+    if (rc == GQA_ERR_CUDA) t_last_cuda_error = cudaGetLastError();
+    return static_cast<gqa_status>(rc);
 }
 
 gqa_status gqa_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new, const void *v_new,
@@ -268,6 +276,11 @@ const char *gqa_status_string(int status) {
         case GQA_ERR_RANGE: return "position beyond the RoPE table";
         default: return "unknown status";
     }
+}
+
+const char *gqa_last_error_string(void) {
+    return t_last_cuda_error == cudaSuccess ? "no CUDA error recorded"
+                                            : cudaGetErrorString(t_last_cuda_error);
 }
 
 gqa_status gqa_device_check(void) {

@@ -13,11 +13,13 @@
 // §1 and §5.3: local prefill costs O(T W)); the per-element mask is applied on the tiles
 // that straddle the diagonal or the window's lower edge only.
 //
-// Warp roles (12 warps):
+// Warp roles (12 warps, 3 warpgroups):
 //   warp 0      TMA producer: Q tiles once, then K/V tiles into a 2-stage ring.
 //   warp 1      tensor-memory allocator and the single MMA-issuing thread.
-//   warps 4-7   softmax for query tile 0 (thread = row = TMEM lane);
-//   warps 8-11  softmax for query tile 1.
+//   warps 2-3   idle (with 12 warps, 3 per SM sub-partition, every thread gets 168
+//               registers; fewer warps would not raise that cap).
+//   warps 4-7   softmax for query tile 0, warps 8-11 for query tile 1: one thread per
+//               query row; warp w reads TMEM lanes 32*(w%4).. (its lane quarter).
 // Q is rotated (RoPE, §6.1) in shared memory by the softmax warps right after it lands;
 // K arrives already rotated (the caller-side pass rotates each key once).
 //
@@ -296,6 +298,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < n_tiles; ++j) {
                 if (!warp_wait(&bars->s_full[wg], j & 1)) { ok = false; break; }
                 tc_fence_after();
+                const int n0 = (kt_first + j) * kBN;
+                const bool full = valid && (n0 + kBN - 1 <= qpos) &&
+                                  (p.window <= 0 || n0 >= qpos - p.window + 1);
+                // visible columns of this row in the tile: [c_lo, c_hi)
+                int c_lo = 0, c_hi = kBN;
+                if (!full) {
+                    c_hi = valid ? min(kBN, qpos - n0 + 1) : 0;
+                    c_lo = p.window > 0 ? max(0, qpos - p.window + 1 - n0) : 0;
+                }
+                // the whole S row in registers: four loads in flight, one wait
                 float x[128];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -305,26 +317,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(rr[i]);
                 }
                 tmem_wait_ld();
-                const int n0 = (kt_first + j) * kBN;
-                const bool full = valid && (n0 + kBN - 1 <= qpos) &&
-                                  (p.window <= 0 || n0 >= qpos - p.window + 1);
-                float mx = -CUDART_INF_F;
-                if (full) {
+                if (!full) {
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        x[c] *= p.scale_log2;
-                        mx = fmaxf(mx, x[c]);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        const int kpos = n0 + c;
-                        const bool vis = valid && kpos <= qpos &&
-                                         (p.window <= 0 || qpos - kpos < p.window);
-                        x[c] = vis ? x[c] * p.scale_log2 : -CUDART_INF_F;
-                        mx = fmaxf(mx, x[c]);
-                    }
+                    for (int i = 0; i < 128; ++i)
+                        x[i] = (i >= c_lo && i < c_hi) ? x[i] : -CUDART_INF_F;
                 }
+                // row maximum of the raw scores: 3-input max, 8 independent chains of 16
+                float mx8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    mx8[k] = fmax3(x[k], x[k + 8], x[k + 16]);
+#pragma unroll
+                    for (int t = 3; t < 15; t += 2)
+                        mx8[k] = fmax3(mx8[k], x[k + 8 * t], x[k + 8 * t + 8]);
+                    mx8[k] = fmaxf(mx8[k], x[k + 120]);
+                }
+                const float mraw = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                         fmaxf(mx8[6], mx8[7]));
+                const float mx = mraw * p.scale_log2;   // scale > 0: max commutes with it
                 const float m_new = fmaxf(m, mx);
                 const bool grow = m_new > m + kRescaleThreshold;  // false while both -inf
                 const bool need_o = grow && j > 0 && m != -CUDART_INF_F;
@@ -333,26 +343,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l *= f;
                     m = m_new;
                 }
-                const float mref = (m == -CUDART_INF_F) ? 0.f : m;
-                {
-                    uint32_t pk[32];
+                const float nmref = (m == -CUDART_INF_F) ? 0.f : -m;
+                // P = 2^(s * scale * log2e - m) as bf16 over the first 64 columns of the S
+                // tile, 16 columns at a time (each piece lands on columns already read);
+                // packed fp32x2 FMA / add, row sum in 4 pairs of chains
+                float2 ls[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float e0 = ex2_approx(x[2 * i] - mref);
-                        const float e1 = ex2_approx(x[2 * i + 1] - mref);
-                        l += e0 + e1;
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 a = ffma2(make_float2(x[32 * c + 2 * i], x[32 * c + 2 * i + 1]),
+                                               p.scale_log2, nmref);
+                        const float e0 = ex2_approx(a.x), e1 = ex2_approx(a.y);
+                        ls[i & 3] = fadd2(ls[i & 3], make_float2(e0, e1));
                         pk[i] = pack_bf16x2(e0, e1);
                     }
-                    tmem_st32(tS, pk);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float e0 = ex2_approx(x[64 + 2 * i] - mref);
-                        const float e1 = ex2_approx(x[64 + 2 * i + 1] - mref);
-                        l += e0 + e1;
-                        pk[i] = pack_bf16x2(e0, e1);
-                    }
-                    tmem_st32(tS + 32, pk);
+                    tmem_st16(tS + 16 * c, pk);
                 }
+                l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) +
+                     ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
                 if (__any_sync(0xffffffffu, need_o)) {
                     // O still holds the product of tiles < j: wait for the last one, then
                     // rescale it in TMEM before this tile's PV is issued.
@@ -465,7 +475,7 @@ int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, flo
     if (!attr_done) {
         if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess)
-            return GQA_ERR_CUDA;
+            return GQA_ERR_CUDA;   // the error stays readable with cudaGetLastError
         attr_done = true;
     }
     Params p;
@@ -484,7 +494,8 @@ int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, flo
     p.scale_log2 = scale * 1.4426950408889634f;
     const long nblocks = (long)B * Hkv * p.n_pairs * p.n_mblocks;
     prefill_kernel<<<static_cast<unsigned>(nblocks), kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
-    return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    const cudaError_t e = cudaPeekAtLastError();
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 }  // namespace gqa

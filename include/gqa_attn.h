@@ -186,6 +186,10 @@ gqa_status gqa_get_device_status(gqa_stream_t stream);
 /* Static, human-readable text for a status code. */
 const char *gqa_status_string(int status);
 
+/* Text of the CUDA runtime error behind the most recent GQA_ERR_CUDA returned to the
+ * calling host thread (static storage; "no CUDA error recorded" if there was none). */
+const char *gqa_last_error_string(void);
+
 /* GQA_OK if the current CUDA device is an sm_103 part this build can run on. */
 gqa_status gqa_device_check(void);
 
