@@ -223,24 +223,29 @@ def prefill_setup(layer):
     return st
 
 
-def bench_prefill(layer, steps: int, warmup: int, stream, peaks, peak_src, world,
+def bench_prefill(layers, steps: int, warmup: int, stream, peaks, peak_src, world,
                   with_e2e: bool, clocks_index=None):
+    """One step = every layer of the workload in sequence, each = K rotated once
+    (gqa_rope_apply) + the attention kernel (gqa_attn_prefill, k_is_rotated=1)."""
     import torch
     import global_causal_gqa_gb300 as gqa
     from global_causal_gqa_gb300 import accounting as acc
-    L = layer
-    st = prefill_setup(L)
-    flops = acc.prefill_flops(L.B, L.Hq, L.T, L.S, L.d, L.window)
-    timer = Timer(torch, stream, 3)
+    if not isinstance(layers, (list, tuple)):
+        layers = [layers]
+    sts = [prefill_setup(L) for L in layers]
+    flops = sum(acc.prefill_flops(L.B, L.Hq, L.T, L.S, L.d, L.window) for L in layers)
+    timer = Timer(torch, stream, 2 * len(layers) + 1)
 
     def step(mark):
         mark()
-        gqa.gqa_rope_apply(st["k"], st["ws"], L.B, L.Hkv, L.S, L.d, 0, st["table"], L.S, stream)
-        mark()
-        gqa.gqa_attn_prefill(st["q"], st["ws"], st["v"], st["o"], None, L.B, L.T, L.S, L.Hq,
-                             L.Hkv, L.d, L.window, L.scale, st["table"], L.S, 1, None, 0,
-                             stream)
-        mark()
+        for L, st in zip(layers, sts):
+            gqa.gqa_rope_apply(st["k"], st["ws"], L.B, L.Hkv, L.S, L.d, 0, st["table"], L.S,
+                               stream)
+            mark()
+            gqa.gqa_attn_prefill(st["q"], st["ws"], st["v"], st["o"], None, L.B, L.T, L.S,
+                                 L.Hq, L.Hkv, L.d, L.window, L.scale, st["table"], L.S, 1,
+                                 None, 0, stream)
+            mark()
 
     timer.run(warmup, step, timed=False)
     torch.cuda.synchronize()
@@ -261,9 +266,10 @@ def bench_prefill(layer, steps: int, warmup: int, stream, peaks, peak_src, world
     st_code = gqa.gqa_get_device_status(stream)
     assert st_code == 0, f"device status {st_code}"
     dur = timer.durations_ms()
-    step_ms = statistics.mean(a + b for a, b in dur)
-    kern_ms = statistics.mean(b for _, b in dur)
-    rope_ms = statistics.mean(a for a, _ in dur)
+    step_ms = statistics.mean(sum(d) for d in dur)
+    rope_ms = statistics.mean(sum(d[0::2]) for d in dur)
+    kern_ms = statistics.mean(sum(d[1::2]) for d in dur)
+    per_layer = [statistics.mean(d[2 * i + 1] for d in dur) for i in range(len(layers))]
     step_ms_max = max_over_ranks(world, step_ms)
     value = world * flops / (step_ms_max * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
@@ -276,11 +282,22 @@ def bench_prefill(layer, steps: int, warmup: int, stream, peaks, peak_src, world
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"bf16_tflops (burst, {peak_src})",
                      "traffic": traffic_record("prefill_kernel", "prefill.cu")},
-        "gpu_launches": 2 * steps,
+        "gpu_launches": 2 * len(layers) * steps,
         "clocks": sampler.summary() if sampler else None,
     }
+    if len(layers) > 1:
+        out["per_layer"] = [
+            {"d": L.d, "window": L.window, "ms": ms,
+             "tflops": acc.prefill_flops(L.B, L.Hq, L.T, L.S, L.d, L.window) / (ms * 1e-3) / 1e12}
+            for L, ms in zip(layers, per_layer)]
+        out["roofline"]["kernel"] = "prefill_kernel / prefill_wide_kernel"
+        out["roofline"]["traffic"] = None
     if with_e2e:
-        out["e2e"] = e2e_prefill(L, st, steps, warmup, stream, flops)
+        out["e2e"] = e2e_prefill(layers[0], sts[0], steps, warmup, stream,
+                                 acc.prefill_flops(layers[0].B, layers[0].Hq, layers[0].T,
+                                                   layers[0].S, layers[0].d, layers[0].window))
+        if len(layers) > 1:
+            out["e2e"]["note"] = "first layer only"
     return out
 
 
@@ -601,14 +618,13 @@ def main():
         main_res = bench_decode(wl, args.steps, args.warmup, stream, peaks, peak_src, world,
                                 True, clock_idx)
     else:
-        if len(wl.layers) != 1:
-            raise SystemExit(f"{wl.name}: multi-layer workloads are not supported yet")
-        main_res = bench_prefill(wl.layers[0], args.steps, args.warmup, stream, peaks,
+        main_res = bench_prefill(list(wl.layers), args.steps, args.warmup, stream, peaks,
                                  peak_src, world, True, clock_idx)
 
     extra = []
     if world == 1 and not args.no_extra:
-        for name in ("plamo3_local_prefill", "plamo3_global_prefill", "plamo3_decode_batch32"):
+        for name in ("plamo3_local_prefill", "plamo3_global_prefill", "plamo3_decode_batch32",
+                     "gemma4_period_6layer"):
             if name == wl.name:
                 continue
             other = get_workload(name)
@@ -616,11 +632,9 @@ def main():
             if isinstance(other, DecodeWorkload):
                 r = bench_decode(other, ks, kw, stream, peaks, peak_src, 1, False)
             else:
-                r = bench_prefill(other.layers[0], ks, kw, stream, peaks, peak_src, 1, False)
+                r = bench_prefill(list(other.layers), ks, kw, stream, peaks, peak_src, 1, False)
             r.pop("clocks", None)
             extra.append({"workload": name, "steps": ks, "warmup": kw, **r})
-        extra.append({"workload": "gemma4_period_6layer",
-                      "unsupported": "head dims 256/512 not built yet"})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

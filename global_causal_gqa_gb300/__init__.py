@@ -24,7 +24,7 @@ __all__ = [
     "gqa_rope_inv_freq", "gqa_yarn_amplitude", "gqa_rope_table_bytes", "gqa_rope_table_build",
     "gqa_rope_apply", "gqa_prefill_workspace_bytes", "gqa_attn_prefill", "gqa_kv_append",
     "gqa_decode_workspace_bytes", "gqa_attn_decode", "gqa_attn_decode_static",
-    "gqa_get_device_status",
+    "gqa_get_device_status", "gqa_get_device_diag",
     "gqa_status_string", "gqa_last_error_string", "gqa_device_check",
 ]
 
@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
             "gqa_attn_decode": ([P, P, I, I, I, I, F, I, P, P, P, Z, P], I),
             "gqa_attn_decode_static": ([P, P, I, I, I, I, F, I, P, P, P], I),
             "gqa_get_device_status": ([P], I),
+            "gqa_get_device_diag": ([P, P, I], I),
             "gqa_status_string": ([I], ctypes.c_char_p),
             "gqa_last_error_string": ([], ctypes.c_char_p),
             "gqa_device_check": ([], I),
@@ -216,6 +217,14 @@ def gqa_attn_decode_static(q, descs, nseq: int, Hq: int, Hkv: int, d: int, scale
 
 def gqa_get_device_status(stream=None) -> int:
     return lib().gqa_get_device_status(_stream(stream))
+
+
+def gqa_get_device_diag(stream=None) -> list:
+    """Diagnostic codes of the device-side waits that expired (first overall, then the
+    first of each kernel role 0-3; 0 where none); cleared by the read."""
+    v = (ctypes.c_int32 * 5)()
+    _check("gqa_get_device_diag", lib().gqa_get_device_diag(_stream(stream), v, 5), True)
+    return list(v)
 
 
 def gqa_status_string(status: int) -> str:

@@ -18,7 +18,9 @@ constexpr int kMaxDevices = 64;
 
 // One status word per device.  Kernels record the first device-side error here with
 // atomicCAS; gqa_get_device_status reads and clears it.
-__device__ int g_status_word;
+// Word 0: status; word 1: diagnostic code of the first device-side wait that expired;
+// words 2-5: the first expired wait of each kernel role (0-3).
+__device__ int g_status_word[6];
 
 int *status_ptr() {
     static std::mutex mu;
@@ -91,7 +93,8 @@ size_t gqa_rope_table_bytes(int d, int max_pos) {
 
 gqa_status gqa_rope_table_build(float *table, const double *inv_freq, int d, double amp,
                                 int max_pos, gqa_stream_t stream) {
-    if (!table || !inv_freq || !rope_dim_ok(d) || max_pos <= 0 || !std::isfinite(amp))
+    if (!table || !inv_freq || !rope_dim_ok(d) || max_pos <= 0 || !std::isfinite(amp) ||
+        !(amp > 0.0))
         return GQA_ERR_INVALID_ARG;
     if (!aligned16(table)) return GQA_ERR_ALIGNMENT;
     gqa::InvFreq w{};
@@ -126,7 +129,7 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
     if (!q || !k || !v || !o || !table || B <= 0 || T <= 0 || S <= 0 || T > S || Hq <= 0 ||
         Hkv <= 0 || (Hq % Hkv) != 0 || !std::isfinite(scale))
         return GQA_ERR_INVALID_ARG;
-    if (d != 128) return GQA_ERR_UNSUPPORTED;
+    if (d != 128 && d != 256 && d != 512) return GQA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(table) ||
         (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return GQA_ERR_ALIGNMENT;
@@ -136,8 +139,11 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
         if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
         if (!aligned16(workspace)) return GQA_ERR_ALIGNMENT;
     }
-    // the grid is one CTA per (b, KV head, head pair, 128-row block)
-    const long blocks = static_cast<long>(B) * Hkv * ((Hq / Hkv + 1) / 2) * ((T + 127) / 128);
+    // the grid: one CTA per (b, KV head, head pair, 128-row block) for d = 128, per
+    // (b, head, 128-row block, output slice) for d = 256 / 512
+    const long mblocks = (T + 127) / 128;
+    const long blocks = d == 128 ? static_cast<long>(B) * Hkv * ((Hq / Hkv + 1) / 2) * mblocks
+                                 : static_cast<long>(B) * Hq * mblocks * (d == 512 ? 2 : 1);
     if (blocks > 0x7fffffffL) return GQA_ERR_UNSUPPORTED;
     int *st = status_ptr();
     if (!st) return GQA_ERR_CUDA;
@@ -151,8 +157,10 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
         if (e != cudaSuccess) return GQA_ERR_CUDA;
         k_rot = workspace;
     }
-    const int rc = gqa::launch_prefill(q, k_rot, v, o, lse, B, T, S, Hq, Hkv, d, window, scale,
-                                       table, table_len, st, s);
+    const int rc = d == 128 ? gqa::launch_prefill(q, k_rot, v, o, lse, B, T, S, Hq, Hkv, d,
+                                                  window, scale, table, table_len, st, s)
+                            : gqa::launch_prefill_wide(q, k_rot, v, o, lse, B, T, S, Hq, Hkv,
+                                                       d, window, scale, table, st, s);
     if (rc == GQA_ERR_CUDA) t_last_cuda_error = cudaGetLastError();
     return static_cast<gqa_status>(rc);
 }
@@ -261,6 +269,22 @@ gqa_status gqa_get_device_status(gqa_stream_t stream) {
             return GQA_ERR_CUDA;
     }
     return static_cast<gqa_status>(v);
+}
+
+gqa_status gqa_get_device_diag(gqa_stream_t stream, int32_t *diag, int n) {
+    if (!diag || n <= 0) return GQA_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    int v[5] = {0, 0, 0, 0, 0};
+    if (cudaMemcpy(v, st + 1, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    for (int i = 0; i < n; ++i) diag[i] = i < 5 ? v[i] : 0;
+    const int zero[5] = {0, 0, 0, 0, 0};
+    if (cudaMemcpy(st + 1, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return GQA_ERR_CUDA;
+    return GQA_OK;
 }
 
 const char *gqa_status_string(int status) {

@@ -6,7 +6,8 @@
 // 4 Hkv d bytes per token and layer -- the bound this kernel is written against).
 //
 // Work split: one CTA per (split of kDecodeChunk keys, sequence, block of <= 8 KV heads);
-// one warp per KV head streams its keys in blocks of 16 with 16-byte read-only loads.
+// one warp per KV head streams its keys in blocks of 16 with 16-byte read-only loads,
+// double-buffered in registers so the next block's loads are in flight during the math.
 // The query group of G <= 8 heads shares every K and V element, so the per-block math
 // is two warp-level bf16 MMAs (m16n8k16): S^T = K' Q'^T and O^T += V^T P^T, fp32
 // accumulate.  The head dimension is permuted (identically on both operands of each
@@ -96,7 +97,7 @@ __device__ __forceinline__ SeqView seq_view(const gqa_kv_desc &desc, int max_len
     return v;
 }
 
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 1)
     decode_partial_kernel(const __nv_bfloat16 *__restrict__ q,
                           const gqa_kv_desc *__restrict__ descs, int Hq, int Hkv,
                           float scale_log2, int max_len, int nsplit, float *__restrict__ ws_ml,
@@ -158,41 +159,52 @@ __global__ void __launch_bounds__(kWarps * 32)
         return s >= sv.cap ? s - sv.cap : s;
     };
 
-    for (int kb = k_start; kb < k_end; kb += 16) {
-        // K rows kb + gq and kb + gq + 8; V rows kb + 2tq + {0, 1, 8, 9} (clamped in range;
-        // keys at or past k_end get weight 0).
-        const int key0 = kb + gq, key1 = kb + gq + 8;
-        const bool ok0 = key0 < k_end, ok1 = key1 < k_end;
-        const int kk0 = ok0 ? key0 : k_end - 1, kk1 = ok1 ? key1 : k_end - 1;
+    // One block = 16 keys: K rows kb + gq and kb + gq + 8, V rows kb + 2tq + {0, 1, 8, 9};
+    // rows at or past k_end are clamped in range and get weight 0.  Two register buffers:
+    // the next block's loads are in flight while the current block is computed.
+    struct Block {
+        uint4 k0[4], k1[4], vv[4][2];
+        int kb;
+    };
+    auto load = [&](Block &bl, int kb) {
+        bl.kb = kb;
+        const int kk0 = min(kb + gq, k_end - 1), kk1 = min(kb + gq + 8, k_end - 1);
         const uint4 *kr0 = reinterpret_cast<const uint4 *>(kbase + (size_t)slot_of(kk0) * kD);
         const uint4 *kr1 = reinterpret_cast<const uint4 *>(kbase + (size_t)slot_of(kk1) * kD);
-        uint4 k0[4], k1[4], vv[4][2];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            k0[c] = ld_stream(kr0 + 4 * c + tq);
-            k1[c] = ld_stream(kr1 + 4 * c + tq);
+            bl.k0[c] = ld_stream(kr0 + 4 * c + tq);
+            bl.k1[c] = ld_stream(kr1 + 4 * c + tq);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            int key = kb + 2 * tq + (i & 1) + ((i >> 1) << 3);
-            key = key < k_end ? key : k_end - 1;
+            const int key = min(kb + 2 * tq + (i & 1) + ((i >> 1) << 3), k_end - 1);
             const uint4 *vr = reinterpret_cast<const uint4 *>(vbase + (size_t)slot_of(key) * kD);
-            vv[i][0] = ld_stream(vr + 2 * gq);
-            vv[i][1] = ld_stream(vr + 2 * gq + 1);
+            bl.vv[i][0] = ld_stream(vr + 2 * gq);
+            bl.vv[i][1] = ld_stream(vr + 2 * gq + 1);
         }
+    };
+    auto compute = [&](Block &bl) {
+        const int kb = bl.kb;
+        const int key0 = kb + gq, key1 = kb + gq + 8;
+        const bool ok0 = key0 < k_end, ok1 = key1 < k_end;
+        const int kk0 = ok0 ? key0 : k_end - 1, kk1 = ok1 ? key1 : k_end - 1;
         // rotate K at logical positions kk0, kk1
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            rotate8(k0[c], k0[c + 2], table + (size_t)kk0 * (kD / 2) + 32 * c + 8 * tq);
-            rotate8(k1[c], k1[c + 2], table + (size_t)kk1 * (kD / 2) + 32 * c + 8 * tq);
+            rotate8(bl.k0[c], bl.k0[c + 2], table + (size_t)kk0 * (kD / 2) + 32 * c + 8 * tq);
+            rotate8(bl.k1[c], bl.k1[c + 2], table + (size_t)kk1 * (kD / 2) + 32 * c + 8 * tq);
         }
-        // S^T (16 keys x 8 heads)
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T (16 keys x 8 heads) in two independent accumulation chains
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, t[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            mma16816(s, k0[c].x, k1[c].x, k0[c].y, k1[c].y, qb[2 * c][0], qb[2 * c][1]);
-            mma16816(s, k0[c].z, k1[c].z, k0[c].w, k1[c].w, qb[2 * c + 1][0], qb[2 * c + 1][1]);
+            mma16816(s, bl.k0[c].x, bl.k1[c].x, bl.k0[c].y, bl.k1[c].y, qb[2 * c][0], qb[2 * c][1]);
+            mma16816(t, bl.k0[c].z, bl.k1[c].z, bl.k0[c].w, bl.k1[c].w, qb[2 * c + 1][0],
+                     qb[2 * c + 1][1]);
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[i] += t[i];
         // online softmax per head column (heads 2tq, 2tq+1), log2 domain
         const float x0 = ok0 ? s[0] * scale_log2 : -CUDART_INF_F;
         const float x1 = ok0 ? s[1] * scale_log2 : -CUDART_INF_F;
@@ -222,11 +234,21 @@ __global__ void __launch_bounds__(kWarps * 32)
             o[mt][1] *= f1;
             o[mt][2] *= f0;
             o[mt][3] *= f1;
-            const uint32_t w0 = word(vv[0][mt >> 2], mt & 3), w1 = word(vv[1][mt >> 2], mt & 3);
-            const uint32_t w2 = word(vv[2][mt >> 2], mt & 3), w3 = word(vv[3][mt >> 2], mt & 3);
+            const uint32_t w0 = word(bl.vv[0][mt >> 2], mt & 3), w1 = word(bl.vv[1][mt >> 2], mt & 3);
+            const uint32_t w2 = word(bl.vv[2][mt >> 2], mt & 3), w3 = word(bl.vv[3][mt >> 2], mt & 3);
             mma16816(o[mt], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
                      __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), pb0, pb1);
         }
+    };
+
+    Block ba, bb;
+    load(ba, k_start);
+    for (int kb = k_start; kb < k_end; kb += 32) {
+        if (kb + 16 < k_end) load(bb, kb + 16);
+        compute(ba);
+        if (kb + 16 >= k_end) break;
+        if (kb + 32 < k_end) load(ba, kb + 32);
+        compute(bb);
     }
 
     // partial sums of l over the 8 key rows held across gq

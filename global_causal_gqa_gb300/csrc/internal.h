@@ -36,4 +36,9 @@ int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, flo
                    int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
                    const float *table, int table_len, int *status, cudaStream_t s);
 
+// Prefill for d = 256 / 512 (prefill_wide.cu); returns a gqa_status
+int launch_prefill_wide(const void *q, const void *k_rot, const void *v, void *o, float *lse,
+                        int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
+                        const float *table, int *status, cudaStream_t s);
+
 }  // namespace gqa

@@ -227,6 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (i == ntile - 1) umma_commit(&bars->kv_empty[s]);
                     if (j + 1 < n_tiles) {
                         if (i == 0 && !(ok = mbar_wait(&bars->k_full[s1], par1))) break;
+                        // S_i(j+1) overwrites the TMEM columns P_i(j) sits in; the tensor
+                        // pipe does not order that write after PV_i(j)'s read, so wait for
+                        // PV_i(j) to complete first
+                        if (!(ok = mbar_wait(&bars->o_done[i], j & 1))) break;
                         tc_fence_after();
                         issue_s(i, s1);
                     }

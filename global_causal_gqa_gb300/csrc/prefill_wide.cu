@@ -1,0 +1,529 @@
+// prefill_wide.cu -- causal / sliding-window GQA prefill for wide heads (d = 256, 512) on
+// tcgen05 tensor cores.
+//
+// Same computation as prefill.cu ("PLaMo 3アーキテクチャ徹底解析" §4.5, §5.1; the
+// Gemma-4 shapes of the qiita.com Gemma-4-26B-A4B explainer, Attention block section, and
+// the p-RoPE of §6.4), for heads too wide for two query tiles to share tensor memory:
+// a 128 x d fp32 output tile alone takes d of the 512 TMEM columns.
+//
+// CTA = (batch, query head, 128-row query block, output slice).  One query tile per CTA;
+// its score tile S is double-buffered in TMEM so that S(j+1) = Q K(j+1)^T runs on the
+// tensor core while the softmax warps work on S(j).  TMEM: S_a, S_b (BN columns each) and
+// O (DV columns).  K streams through a ring of 128-dim chunks (TMA, 128-byte swizzle), V
+// (only the DV output columns of this CTA) through its own ring.
+//   d = 256: BN = 128, DV = 256: 128 + 128 + 256 = 512 columns.
+//   d = 512: BN = 64, DV = 256, two output slices per query tile: both CTAs of a pair
+//            compute the full S (the score contraction runs over all 512 dims) and each
+//            accumulates half of O -- 64 + 64 + 256 = 384 columns.
+// Warps: 0 TMA producer of Q and K, 1 TMEM owner + MMA issuer, 2 TMA producer of V,
+// 3 idle, 4-7 softmax/epilogue (one thread per query row).  Q is rotated (RoPE) in shared memory after it lands; pairs
+// (j, j + d/2) sit at the same offset of boxes k and k + d/128.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+template <int D>
+struct Wide;
+
+template <>
+struct Wide<256> {
+    static constexpr int BN = 128, DV = 256, KST = 2, VST = 1;
+};
+template <>
+struct Wide<512> {
+    static constexpr int BN = 64, DV = 256, KST = 4, VST = 1;
+};
+
+struct WBars {
+    uint64_t q_full, q_ready;
+    uint64_t k_full[4], k_empty[4];
+    uint64_t v_full[2], v_empty[2];
+    uint64_t s_full[2], p_full[2], o_done, mma_done;
+    uint32_t tmem_base;
+};
+
+struct WParams {
+    __nv_bfloat16 *o;
+    float *lse;
+    const float2 *table;
+    int *status;
+    int T, S, Hq, Hkv, G, window;
+    int n_mblocks, n_slices;
+    float scale_log2;
+};
+
+__device__ __forceinline__ bool warp_wait_w(uint64_t *bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const WParams p) {
+    constexpr int BN = Wide<D>::BN, DV = Wide<D>::DV, KST = Wide<D>::KST, VST = Wide<D>::VST;
+    constexpr int NKC = D / 128;                  // 128-dim K chunks per key tile
+    constexpr int QBOX = kBM * 128;               // 128 rows x 64 bf16
+    constexpr int QBYTES = (D / 64) * QBOX;
+    constexpr int KBOX = BN * 128;                // BN rows x 64 bf16
+    constexpr int KCHUNK = 2 * KBOX;              // BN rows x 128 bf16
+    constexpr int VTILE = (DV / 64) * KBOX;       // BN rows x DV bf16
+    constexpr int OFF_K = QBYTES;
+    constexpr int OFF_V = OFF_K + KST * KCHUNK;
+    constexpr int OFF_BAR = OFF_V + VST * VTILE;
+    constexpr uint32_t TS0 = 0, TS1 = BN, TO = 2 * BN;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    WBars *bars = reinterpret_cast<WBars *>(smem + OFF_BAR);
+    uint8_t *sQ = smem;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int idx = blockIdx.x;
+    const int slice = idx % p.n_slices;
+    idx /= p.n_slices;
+    const int h = idx % p.Hq;
+    idx /= p.Hq;
+    const int mb = p.n_mblocks - 1 - (idx % p.n_mblocks);   // longest rows first
+    const int b = idx / p.n_mblocks;
+    const int g = h / p.G;
+    const int q_lo = p.S - p.T + mb * kBM;
+    const int q_hi = min(q_lo + kBM - 1, p.S - 1);
+    const int kt_first = p.window > 0 ? max(0, q_lo - p.window + 1) / BN : 0;
+    const int n_tiles = q_hi / BN - kt_first + 1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_ready, 128);
+        for (int i = 0; i < KST; ++i) {
+            mbar_init(&bars->k_full[i], 1);
+            mbar_init(&bars->k_empty[i], 1);
+        }
+        for (int i = 0; i < VST; ++i) {
+            mbar_init(&bars->v_full[i], 1);
+            mbar_init(&bars->v_empty[i], 1);
+        }
+        mbar_init(&bars->s_full[0], 1);
+        mbar_init(&bars->s_full[1], 1);
+        mbar_init(&bars->p_full[0], 128);
+        mbar_init(&bars->p_full[1], 128);
+        mbar_init(&bars->o_done, 1);
+        mbar_init(&bars->mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        // ================= TMA producer: Q, then K chunks =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            const int zq = b * p.Hq + h, zk = b * p.Hkv + g;
+            mbar_arrive_expect_tx(&bars->q_full, QBYTES);
+            for (int i = 0; i < D / 64; ++i)
+                tma_load_3d(sQ + i * QBOX, &tmQ, &bars->q_full, 64 * i, mb * kBM, zq);
+            bool ok = true;
+            int issued = 0;
+            for (int u = 0; u < n_tiles * NKC && ok; ++u) {
+                const int j = u / NKC, c = u % NKC, st = u % KST;
+                if (u >= KST && !(ok = mbar_wait(&bars->k_empty[st], ((u / KST) - 1) & 1))) {
+                    set_timeout(p.status, kDiagPrefillWide, 0, 1, u);
+                    break;
+                }
+                const int n0 = (kt_first + j) * BN;
+                uint8_t *dst = smem + OFF_K + st * KCHUNK;
+                mbar_arrive_expect_tx(&bars->k_full[st], KCHUNK);
+                tma_load_3d(dst, &tmK, &bars->k_full[st], 128 * c, n0, zk);
+                tma_load_3d(dst + KBOX, &tmK, &bars->k_full[st], 128 * c + 64, n0, zk);
+                issued = u + 1;
+            }
+            if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
+            // never leave the CTA with copies in flight
+            mbar_wait(&bars->q_full, 0);
+            for (int u = max(0, issued - KST); u < issued; ++u)
+                mbar_wait(&bars->k_full[u % KST], (u / KST) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ================= TMA producer: V (this CTA's output columns) =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmV);
+            const int zk = b * p.Hkv + g;
+            bool ok = true;
+            int issued = 0;
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int vs = j % VST;
+                if (j >= VST && !(ok = mbar_wait(&bars->v_empty[vs], ((j / VST) - 1) & 1))) {
+                    set_timeout(p.status, kDiagPrefillWide, 2, 3, j);
+                    break;
+                }
+                const int n0 = (kt_first + j) * BN;
+                uint8_t *dst = smem + OFF_V + vs * VTILE;
+                mbar_arrive_expect_tx(&bars->v_full[vs], VTILE);
+                for (int i = 0; i < DV / 64; ++i)
+                    tma_load_3d(dst + i * KBOX, &tmV, &bars->v_full[vs], slice * DV + 64 * i, n0,
+                                zk);
+                issued = j + 1;
+            }
+            if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
+            for (int j = max(0, issued - VST); j < issued; ++j)
+                mbar_wait(&bars->v_full[j % VST], (j / VST) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
+            const uint32_t idesc_o = idesc_bf16_f32(kBM, DV, 0, 1);
+            const uint32_t qaddr = smem_u32(sQ);
+            const uint32_t kaddr = smem_u32(smem + OFF_K), vaddr = smem_u32(smem + OFF_V);
+            bool ok = mbar_wait(&bars->q_ready, 0);
+            if (!ok) set_timeout(p.status, kDiagPrefillWide, 1, 4, 0);
+            tc_fence_after();
+            auto issue_s = [&](int j) {
+                const uint32_t dst = tmem + ((j & 1) ? TS1 : TS0);
+                for (int c = 0; c < NKC && ok; ++c) {
+                    const int u = j * NKC + c, st = u % KST;
+                    if (!(ok = mbar_wait(&bars->k_full[st], (u / KST) & 1))) {
+                        set_timeout(p.status, kDiagPrefillWide, 1, 0, u);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ka = kaddr + st * KCHUNK;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const int dk = 8 * c + kk;   // 16-dim step over the whole head
+                        const uint64_t ad = sdesc_sw128(
+                            qaddr + (dk >> 2) * QBOX + (dk & 3) * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(
+                            ka + (kk >> 2) * KBOX + (kk & 3) * 32, 16, 1024);
+                        umma_ss(dst, ad, bd, idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&bars->k_empty[st]);
+                }
+                if (ok) umma_commit(&bars->s_full[j & 1]);
+            };
+            if (ok) issue_s(0);
+            if (ok && n_tiles > 1) issue_s(1);
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int vs = j % VST;
+                if (!(ok = mbar_wait(&bars->v_full[vs], (j / VST) & 1))) {
+                    set_timeout(p.status, kDiagPrefillWide, 1, 2, j);
+                    break;
+                }
+                // one barrier per S buffer: the softmax may finish S(j+1) before this wait,
+                // never S(j+2) (issued below, after PV(j)), so no phase is skipped
+                if (!(ok = mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1))) {
+                    set_timeout(p.status, kDiagPrefillWide, 1, 5, j);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t pcol = tmem + ((j & 1) ? TS1 : TS0);
+                const uint32_t va = vaddr + vs * VTILE;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    umma_ts(tmem + TO, pcol + kk * 8, sdesc_sw128(va + kk * 2048, KBOX, 1024),
+                            idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bars->o_done);
+                umma_commit(&bars->v_empty[vs]);
+                // S(j+2) reuses the TMEM buffer P(j) sits in: PV(j) must have finished
+                // reading P(j) before the first S(j+2) product is written there
+                if (j + 2 < n_tiles) {
+                    if (!(ok = mbar_wait(&bars->o_done, j & 1))) {
+                        set_timeout(p.status, kDiagPrefillWide, 1, 7, j);
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s(j + 2);
+                }
+            }
+            if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
+            umma_commit(&bars->mma_done);
+            mbar_wait(&bars->mma_done, 0);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ================= softmax / epilogue =================
+        const int r = (warp & 3) * 32 + lane;   // row in tile == TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const int t = mb * kBM + r;
+        const bool valid = t < p.T;
+        const int qpos = p.S - p.T + t;
+        bool ok = warp_wait_w(&bars->q_full, 0);
+        if (!ok) set_timeout(p.status, kDiagPrefillWide, 3, 8, 0);
+        if (ok && valid) {
+            // RoPE on the Q row: pair (j, j + D/2) = same swizzled offset in boxes k, k + D/128
+            const float2 *tab = p.table + (size_t)qpos * (D / 2);
+            for (int kb = 0; kb < D / 128; ++kb) {
+                uint8_t *row0 = sQ + kb * QBOX + r * 128;
+                uint8_t *row1 = row0 + (D / 128) * QBOX;
+#pragma unroll 2
+                for (int c = 0; c < 8; ++c) {
+                    const int pc = (c ^ (r & 7)) * 16;
+                    uint4 a = *reinterpret_cast<uint4 *>(row0 + pc);
+                    uint4 bq = *reinterpret_cast<uint4 *>(row1 + pc);
+                    const float4 *t4 = reinterpret_cast<const float4 *>(tab + 64 * kb + 8 * c);
+                    float cs[16];
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const float4 tv = __ldg(t4 + qq);
+                        cs[4 * qq] = tv.x;
+                        cs[4 * qq + 1] = tv.y;
+                        cs[4 * qq + 2] = tv.z;
+                        cs[4 * qq + 3] = tv.w;
+                    }
+                    uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const float a0 = bf16lo(aw[qq]), a1 = bf16hi(aw[qq]);
+                        const float b0 = bf16lo(bw[qq]), b1 = bf16hi(bw[qq]);
+                        const float c0 = cs[4 * qq], s0 = cs[4 * qq + 1];
+                        const float c1 = cs[4 * qq + 2], s1 = cs[4 * qq + 3];
+                        aw[qq] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
+                        bw[qq] = pack_bf16x2(fmaf(a0, s0, b0 * c0), fmaf(a1, s1, b1 * c1));
+                    }
+                    *reinterpret_cast<uint4 *>(row0 + pc) = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+                    *reinterpret_cast<uint4 *>(row1 + pc) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->q_ready);
+
+        float m = -CUDART_INF_F, l = 0.f;
+        for (int j = 0; j < n_tiles && ok; ++j) {
+            if (!warp_wait_w(&bars->s_full[j & 1], (j >> 1) & 1)) {
+                set_timeout(p.status, kDiagPrefillWide, 3, 6, j);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tS = tmem + lane_off + ((j & 1) ? TS1 : TS0);
+            const int n0 = (kt_first + j) * BN;
+            const bool full = valid && (n0 + BN - 1 <= qpos) &&
+                              (p.window <= 0 || n0 >= qpos - p.window + 1);
+            int c_lo = 0, c_hi = BN;
+            if (!full) {
+                c_hi = valid ? min(BN, qpos - n0 + 1) : 0;
+                c_lo = p.window > 0 ? max(0, qpos - p.window + 1 - n0) : 0;
+            }
+            float x[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(tS + 32 * c, rr);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(rr[i]);
+            }
+            tmem_wait_ld();
+            if (!full) {
+#pragma unroll
+                for (int i = 0; i < BN; ++i) x[i] = (i >= c_lo && i < c_hi) ? x[i] : -CUDART_INF_F;
+            }
+            constexpr int CH = BN / 8;   // values per max chain
+            float mx8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                mx8[k] = x[k];
+#pragma unroll
+                for (int tt = 1; tt < CH; ++tt) mx8[k] = fmaxf(mx8[k], x[k + 8 * tt]);
+            }
+            const float mraw = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                     fmaxf(mx8[6], mx8[7]));
+            const float mx = mraw * p.scale_log2;
+            const float m_new = fmaxf(m, mx);
+            const bool grow = m_new > m + kRescaleThreshold;
+            const bool need_o = grow && j > 0 && m != -CUDART_INF_F;
+            const float f = grow ? ex2_approx(m - m_new) : 1.0f;
+            if (grow) {
+                l *= f;
+                m = m_new;
+            }
+            const float nmref = (m == -CUDART_INF_F) ? 0.f : -m;
+            float2 ls[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float2 a = ffma2(make_float2(x[32 * c + 2 * i], x[32 * c + 2 * i + 1]),
+                                           p.scale_log2, nmref);
+                    const float e0 = ex2_approx(a.x), e1 = ex2_approx(a.y);
+                    ls[i & 3] = fadd2(ls[i & 3], make_float2(e0, e1));
+                    pk[i] = pack_bf16x2(e0, e1);
+                }
+                tmem_st16(tS + 16 * c, pk);
+            }
+            l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) +
+                 ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
+            if (__any_sync(0xffffffffu, need_o)) {
+                // O holds the product of tiles < j: wait for the last one, rescale in TMEM
+                if (!warp_wait_w(&bars->o_done, (j - 1) & 1)) {
+                    set_timeout(p.status, kDiagPrefillWide, 3, 7, j);
+                    ok = false;
+                }
+                tc_fence_after();
+                const float fo = need_o ? f : 1.0f;
+#pragma unroll 1
+                for (int c = 0; c < DV / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tmem + lane_off + TO + 32 * c, rr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        rr[i] = __float_as_uint(__uint_as_float(rr[i]) * fo);
+                    tmem_st32(tmem + lane_off + TO + 32 * c, rr);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bars->p_full[j & 1]);
+        }
+        if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
+        if (ok && warp_wait_w(&bars->o_done, (n_tiles - 1) & 1)) {
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+            __nv_bfloat16 *orow =
+                p.o + (((size_t)b * p.Hq + h) * p.T + t) * D + (size_t)slice * DV;
+#pragma unroll 1
+            for (int c = 0; c < DV / 32; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + lane_off + TO + 32 * c, rr);
+                tmem_wait_ld();
+                if (valid) {
+                    uint32_t pkd[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pkd[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
+                                             __uint_as_float(rr[2 * i + 1]) * inv_l);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2],
+                                            pkd[4 * i + 3]);
+                }
+            }
+            if (valid && p.lse && slice == 0)
+                p.lse[((size_t)b * p.Hq + h) * p.T + t] = (m + __log2f(l)) * 0.69314718055994531f;
+        } else if (ok) {
+            set_timeout(p.status, kDiagPrefillWide, 3, 9, n_tiles);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D>
+constexpr int wide_smem_bytes() {
+    return (D / 64) * kBM * 128 + Wide<D>::KST * 2 * Wide<D>::BN * 128 +
+           Wide<D>::VST * (Wide<D>::DV / 64) * Wide<D>::BN * 128 + 256 + 1024;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn_wide() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// dims {d, rows, slabs}, box {64, box_rows, 1}, 128-byte swizzle
+bool make_map_wide(CUtensorMap *map, const void *base, int d, int rows, int slabs, int box_rows) {
+    EncodeTiledFn fn = encode_fn_wide();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)slabs};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * rows};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+int launch_wide(const void *q, const void *k_rot, const void *v, void *o, float *lse, int B,
+                int T, int S, int Hq, int Hkv, int window, float scale, const float *table,
+                int *status, cudaStream_t s) {
+    constexpr int BN = Wide<D>::BN, DV = Wide<D>::DV;
+    CUtensorMap mq, mk, mv;
+    if (!make_map_wide(&mq, q, D, T, B * Hq, kBM) || !make_map_wide(&mk, k_rot, D, S, B * Hkv, BN) ||
+        !make_map_wide(&mv, v, D, S, B * Hkv, BN))
+        return GQA_ERR_CUDA;
+    constexpr int smem = wide_smem_bytes<D>();
+    static bool attr_done = false;
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(prefill_wide_kernel<D>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return GQA_ERR_CUDA;
+        attr_done = true;
+    }
+    WParams p;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.lse = lse;
+    p.table = reinterpret_cast<const float2 *>(table);
+    p.status = status;
+    p.T = T;
+    p.S = S;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.window = window;
+    p.n_mblocks = (T + kBM - 1) / kBM;
+    p.n_slices = D / DV;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const long nblocks = (long)B * Hq * p.n_mblocks * p.n_slices;
+    prefill_wide_kernel<D><<<static_cast<unsigned>(nblocks), kThreads, smem, s>>>(mq, mk, mv, p);
+    return cudaPeekAtLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_prefill_wide(const void *q, const void *k_rot, const void *v, void *o, float *lse,
+                        int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
+                        const float *table, int *status, cudaStream_t s) {
+    if (d == 256)
+        return launch_wide<256>(q, k_rot, v, o, lse, B, T, S, Hq, Hkv, window, scale, table,
+                                status, s);
+    if (d == 512)
+        return launch_wide<512>(q, k_rot, v, o, lse, B, T, S, Hq, Hkv, window, scale, table,
+                                status, s);
+    return GQA_ERR_UNSUPPORTED;
+}
+
+}  // namespace gqa

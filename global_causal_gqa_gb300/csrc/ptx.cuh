@@ -29,6 +29,18 @@ __device__ __forceinline__ void set_status(int *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// Diagnostic code of the first bounded wait that expired, stored next to the status word:
+// (kernel << 24) | (role << 20) | (barrier << 16) | (tile index & 0xffff).
+enum DiagKernel { kDiagPrefill = 1, kDiagPrefillWide = 2, kDiagDecode = 3 };
+__device__ __forceinline__ void set_timeout(int *status, int kernel, int role, int barrier,
+                                            int tile) {
+    if (!status) return;
+    const int code = (kernel << 24) | (role << 20) | (barrier << 16) | (tile & 0xffff);
+    atomicCAS(status, 0, -6 /* GQA_ERR_DEVICE_TIMEOUT */);
+    atomicCAS(status + 1, 0, code);                // first expired wait overall
+    atomicCAS(status + 2 + (role & 3), 0, code);   // first expired wait of this role
+}
+
 // ---- mbarrier ---------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -85,6 +97,17 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completing `bytes` on the mbarrier.  Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+        "r"(smem_u32(bar))
         : "memory");
 }
 

@@ -27,9 +27,9 @@
  *   - Errors found on the device (a bounded wait that expired, a full cache, an index
  *     out of range) are recorded in the device status word and returned by the next
  *     gqa_get_device_status().  Device code never traps.
- *   - Head dims: prefill d in {128}; decode, kv_append and rope_apply d in {64, 128, 256,
- *     512} (decode: d = 128).  Query group G = Hq/Hkv must be an integer; decode needs
- *     G <= 16.  Other values return GQA_ERR_UNSUPPORTED.
+ *   - Head dims: prefill d in {128, 256, 512}; decode d = 128; kv_append and rope_apply d in
+ *     {64, 128, 256, 512}.  Query group G = Hq/Hkv must be an integer; decode needs
+ *     G <= 8.  Other values return GQA_ERR_UNSUPPORTED.
  */
 #ifndef GQA_ATTN_H
 #define GQA_ATTN_H
@@ -83,7 +83,7 @@ size_t gqa_rope_table_bytes(int d, int max_pos);
  * float pairs table[p*(d/2) + j] = (amp cos(p omega_j), amp sin(p omega_j)) for
  * p < max_pos: the angle and both functions are evaluated in double precision on the
  * device and rounded once to float.  inv_freq: host array of d/2 doubles (see above),
- * copied into the launch, so it may be freed on return.  d <= 512. */
+ * copied into the launch, so it may be freed on return.  d <= 512, amp > 0. */
 gqa_status gqa_rope_table_build(float *table, const double *inv_freq, int d, double amp,
                                 int max_pos, gqa_stream_t stream);
 
@@ -107,7 +107,7 @@ gqa_status gqa_rope_apply(const void *x, void *y, int B, int H, int T, int d, in
  *   gqa_prefill_workspace_bytes(B, Hkv, S, d) bytes; its contents are undefined afterwards.
  * k_is_rotated = 1: k already carries RoPE (a cache that stores rotated keys, as Gemma's
  *   does, §4.4); workspace may be NULL.
- * Supports d = 128.  Hq % Hkv == 0. */
+ * Supports d = 128, 256, 512.  Hq % Hkv == 0. */
 size_t gqa_prefill_workspace_bytes(int B, int Hkv, int S, int d);
 gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o,
                             float *lse, int B, int T, int S, int Hq, int Hkv, int d,
@@ -182,6 +182,14 @@ gqa_status gqa_attn_decode_static(const void *q, const gqa_kv_desc *descs, int n
  * Waits for `stream`, then returns and clears the current device's status word
  * (GQA_OK if no device-side error was recorded since the last call). */
 gqa_status gqa_get_device_status(gqa_stream_t stream);
+
+/* Waits for `stream`, then stores in diag[0..n) and clears the diagnostic codes of the
+ * device-side bounded waits that expired since the last call (0 where none): diag[0] the
+ * first overall, diag[1..4] the first of each kernel role 0..3.  A code is
+ * (kernel << 24) | (role << 20) | (barrier << 16) | (tile index & 0xffff), kernel 1 =
+ * prefill d=128, 2 = prefill d=256/512, 3 = decode.  For diagnosing
+ * GQA_ERR_DEVICE_TIMEOUT; gqa_get_device_status leaves the codes in place. */
+gqa_status gqa_get_device_diag(gqa_stream_t stream, int32_t *diag, int n);
 
 /* Static, human-readable text for a status code. */
 const char *gqa_status_string(int status);

@@ -116,3 +116,35 @@ def test_plamo3_local_prefill_full_size_sampled():
 def test_plamo3_global_prefill_full_size_sampled():
     """B=1, T=S=32768, 64/8 heads, YaRN (s=8), logits x1.2, full causal."""
     _sampled_case(WORKLOADS["plamo3_global_prefill"].layers[0], 4096, 3)
+
+
+# ---- wide heads (Gemma-4 shapes: d = 256 local, d = 512 global with partial RoPE) ----
+PROPE = RopeSpec(base=1e6, rotate_fraction=0.25)
+
+WIDE_CASES = [
+    _layer(1, 200, 200, 2, 1, 0, d=256, seed=61),
+    _layer(1, 130, 130, 4, 2, 1, d=256, seed=62),
+    _layer(1, 300, 300, 4, 2, 64, d=256, seed=63),
+    _layer(2, 257, 257, 4, 4, 127, d=256, seed=64),
+    _layer(1, 100, 333, 6, 2, 0, d=256, seed=65),
+    _layer(1, 200, 200, 2, 1, 0, PROPE, d=512, seed=71),
+    _layer(1, 130, 130, 8, 1, 5, PROPE, d=512, seed=72),
+    _layer(1, 300, 300, 4, 2, 0, PROPE, d=512, seed=73),
+    _layer(1, 65, 500, 8, 2, 100, PROPE, d=512, seed=74),
+    _layer(1, 1, 1, 2, 1, 0, d=512, seed=75),
+]
+
+
+@pytest.mark.parametrize("layer", WIDE_CASES, ids=lambda l: l.label)
+def test_wide_head_edge_cases(layer):
+    _full_case(layer)
+
+
+def test_gemma4_local_layer_full_size_sampled():
+    """T=S=16384, 16 query / 8 KV heads, d=256, window 1024 (layer 0 of the period)."""
+    _sampled_case(WORKLOADS["gemma4_period_6layer"].layers[0], 2048, 4)
+
+
+def test_gemma4_global_layer_full_size_sampled():
+    """T=S=16384, 16 query / 2 KV heads, d=512, full causal, partial RoPE (layer 5)."""
+    _sampled_case(WORKLOADS["gemma4_period_6layer"].layers[5], 1024, 5)
