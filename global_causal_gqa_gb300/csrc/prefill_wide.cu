@@ -51,8 +51,14 @@ struct WBars {
     uint64_t k_full[4], k_empty[4];
     uint64_t v_full[2], v_empty[2];
     uint64_t s_full[2], p_full[2], o_done, mma_done;
+    // the last PV product: S(j+2) waits only for PV(j), so when the softmax finishes the
+    // last tile PV(n-2) may still run and o_done can be two phases behind -- its parity
+    // would then already read as "done" for PV(n-1)
+    uint64_t o_final;
     uint32_t tmem_base;
 };
+
+static_assert(sizeof(WBars) <= 256, "barrier block");
 
 struct WParams {
     __nv_bfloat16 *o;
@@ -121,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->p_full[0], 128);
         mbar_init(&bars->p_full[1], 128);
         mbar_init(&bars->o_done, 1);
+        mbar_init(&bars->o_final, 1);
         mbar_init(&bars->mma_done, 1);
         fence_mbar_init();
     }
@@ -245,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_ts(tmem + TO, pcol + kk * 8, sdesc_sw128(va + kk * 2048, KBOX, 1024),
                             idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&bars->o_done);
+                if (j == n_tiles - 1) umma_commit(&bars->o_final);
                 umma_commit(&bars->v_empty[vs]);
                 // S(j+2) reuses the TMEM buffer P(j) sits in: PV(j) must have finished
                 // reading P(j) before the first S(j+2) product is written there
@@ -400,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bars->p_full[j & 1]);
         }
         if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
-        if (ok && warp_wait_w(&bars->o_done, (n_tiles - 1) & 1)) {
+        if (ok && warp_wait_w(&bars->o_final, 0)) {
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.0f / l : 0.f;
             __nv_bfloat16 *orow =

@@ -148,3 +148,21 @@ def test_gemma4_local_layer_full_size_sampled():
 def test_gemma4_global_layer_full_size_sampled():
     """T=S=16384, 16 query / 2 KV heads, d=512, full causal, partial RoPE (layer 5)."""
     _sampled_case(WORKLOADS["gemma4_period_6layer"].layers[5], 1024, 5)
+
+
+@pytest.mark.parametrize("name,index", [("plamo3_local_prefill", 0),
+                                        ("gemma4_period_6layer", 0),
+                                        ("gemma4_period_6layer", 5)])
+def test_full_size_repeat_bitwise(name, index):
+    """Full-size launches repeated back to back give bit-identical outputs: a result that
+    depended on the timing of the asynchronous pipeline (a barrier phase observed too
+    early, a buffer overwritten while still being read) would show up as a difference."""
+    gu.require_gpu()
+    layer = WORKLOADS[name].layers[index]
+    x = prefill_inputs(layer)
+    q, k, v = gu.to_cuda(x.q, x.k, x.v)
+    table = gu.rope_table(layer.d, layer.rope, layer.S)
+    first, first_lse = gu.run_prefill(q, k, v, layer.window, layer.scale, table, layer.S)
+    for _ in range(6):
+        o, lse = gu.run_prefill(q, k, v, layer.window, layer.scale, table, layer.S)
+        assert torch.equal(o, first) and torch.equal(lse, first_lse)
