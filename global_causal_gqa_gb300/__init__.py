@@ -24,7 +24,7 @@ __all__ = [
     "gqa_rope_inv_freq", "gqa_yarn_amplitude", "gqa_rope_table_bytes", "gqa_rope_table_build",
     "gqa_rope_apply", "gqa_prefill_workspace_bytes", "gqa_attn_prefill", "gqa_kv_append",
     "gqa_decode_workspace_bytes", "gqa_attn_decode", "gqa_attn_decode_static",
-    "gqa_get_device_status", "gqa_get_device_diag",
+    "gqa_get_device_status", "gqa_get_device_diag", "gqa_watchdog_selftest",
     "gqa_status_string", "gqa_last_error_string", "gqa_device_check",
 ]
 
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
             "gqa_attn_decode_static": ([P, P, I, I, I, I, F, I, P, P, P], I),
             "gqa_get_device_status": ([P], I),
             "gqa_get_device_diag": ([P, P, I], I),
+            "gqa_watchdog_selftest": ([ctypes.c_int64, P], I),
             "gqa_status_string": ([I], ctypes.c_char_p),
             "gqa_last_error_string": ([], ctypes.c_char_p),
             "gqa_device_check": ([], I),
@@ -225,6 +226,13 @@ def gqa_get_device_diag(stream=None) -> list:
     v = (ctypes.c_int32 * 5)()
     _check("gqa_get_device_diag", lib().gqa_get_device_diag(_stream(stream), v, 5), True)
     return list(v)
+
+
+def gqa_watchdog_selftest(limit_ns: int, stream=None, check: bool = True) -> int:
+    """Enqueues a wait that nothing completes, bounded by limit_ns; the device records
+    GQA_ERR_DEVICE_TIMEOUT, read back by gqa_get_device_status."""
+    st = lib().gqa_watchdog_selftest(int(limit_ns), _stream(stream))
+    return _check("gqa_watchdog_selftest", st, check)
 
 
 def gqa_status_string(status: int) -> str:

@@ -287,6 +287,14 @@ gqa_status gqa_get_device_diag(gqa_stream_t stream, int32_t *diag, int n) {
     return GQA_OK;
 }
 
+gqa_status gqa_watchdog_selftest(int64_t limit_ns, gqa_stream_t stream) {
+    if (limit_ns < 1000 || limit_ns > 2000000000LL) return GQA_ERR_INVALID_ARG;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    return from_cuda(
+        gqa::launch_watchdog_selftest(limit_ns, st, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char *gqa_status_string(int status) {
     switch (status) {
         case GQA_OK: return "ok";

@@ -41,4 +41,7 @@ int launch_prefill_wide(const void *q, const void *k_rot, const void *v, void *o
                         int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
                         const float *table, int *status, cudaStream_t s);
 
+// Bounded-wait self-test (watchdog.cu)
+cudaError_t launch_watchdog_selftest(int64_t limit_ns, int *status, cudaStream_t s);
+
 }  // namespace gqa

@@ -53,6 +53,14 @@ constexpr int kSmemBytes = kSmemBar + 256 + 1024;  // + barriers + alignment sla
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
+// Column pairs (bit i: pair i of each 32-column chunk) whose exponentials run on the FMA
+// pipe (ex2_fma2) instead of the special-function unit.  Off by default: the softmax is
+// bound by instruction issue and latency, not by the special-function unit, so the
+// extra instructions cost more than the offload saves (measured on GB300).
+#ifndef GQA_PREFILL_POLY_PAIRS
+#define GQA_PREFILL_POLY_PAIRS 0x0000u
+#endif
+constexpr uint32_t kPolyPairs = GQA_PREFILL_POLY_PAIRS;
 
 struct Bars {
     uint64_t q_full;
@@ -259,21 +267,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tile_on) {
             // ---- RoPE on the Q row in shared memory (128-byte swizzle: 16-byte chunk c of
             // row r sits at chunk c ^ (r & 7); pair (j, j + 64) = same offset in box 0 / 1)
+            // the row's table entries are fetched while the Q tile is still in flight
+            float4 tq[32];
+            {
+                const float4 *t4 = reinterpret_cast<const float4 *>(
+                    p.table + (size_t)(valid ? qpos : 0) * (kD / 2));
+#pragma unroll
+                for (int i = 0; i < 32; ++i) tq[i] = __ldg(t4 + i);
+            }
             ok = warp_wait(&bars->q_full, 0);
             if (ok && valid) {
                 uint8_t *row0 = sQ[wg] + r * 128;
                 uint8_t *row1 = row0 + kBoxBytes;
-                const float2 *tab = p.table + (size_t)qpos * (kD / 2);
-#pragma unroll 2
+#pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const int pc = (c ^ (r & 7)) * 16;
                     uint4 a = *reinterpret_cast<uint4 *>(row0 + pc);
                     uint4 bq = *reinterpret_cast<uint4 *>(row1 + pc);
-                    const float4 *t4 = reinterpret_cast<const float4 *>(tab + 8 * c);
                     float cs[16];
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) {
-                        const float4 tv = __ldg(t4 + qq);
+                        const float4 tv = tq[4 * c + qq];
                         cs[4 * qq] = tv.x;
                         cs[4 * qq + 1] = tv.y;
                         cs[4 * qq + 2] = tv.z;
@@ -359,7 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 16; ++i) {
                         const float2 a = ffma2(make_float2(x[32 * c + 2 * i], x[32 * c + 2 * i + 1]),
                                                p.scale_log2, nmref);
-                        const float e0 = ex2_approx(a.x), e1 = ex2_approx(a.y);
+                        float e0, e1;
+                        if ((kPolyPairs >> i) & 1) {
+                            const float2 e = ex2_fma2(a);
+                            e0 = e.x;
+                            e1 = e.y;
+                        } else {
+                            e0 = ex2_approx(a.x);
+                            e1 = ex2_approx(a.y);
+                        }
                         ls[i & 3] = fadd2(ls[i & 3], make_float2(e0, e1));
                         pk[i] = pack_bf16x2(e0, e1);
                     }

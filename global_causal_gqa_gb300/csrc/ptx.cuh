@@ -31,7 +31,7 @@ __device__ __forceinline__ void set_status(int *status, int code) {
 
 // Diagnostic code of the first bounded wait that expired, stored next to the status word:
 // (kernel << 24) | (role << 20) | (barrier << 16) | (tile index & 0xffff).
-enum DiagKernel { kDiagPrefill = 1, kDiagPrefillWide = 2, kDiagDecode = 3 };
+enum DiagKernel { kDiagPrefill = 1, kDiagPrefillWide = 2, kDiagDecode = 3, kDiagWatchdog = 4 };
 __device__ __forceinline__ void set_timeout(int *status, int kernel, int role, int barrier,
                                             int tile) {
     if (!status) return;
@@ -74,14 +74,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if it did not
-// complete within GQA_WAIT_LIMIT_NS.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// complete within limit_ns nanoseconds.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity,
+                                              uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > GQA_WAIT_LIMIT_NS) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// mbar_wait_for with the library-wide limit, GQA_WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, GQA_WAIT_LIMIT_NS);
 }
 
 // ---- TMA ----------------------------------------------------------------------------
@@ -288,6 +294,52 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
         : "=f"(r.x), "=f"(r.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return r;
+}
+
+// Packed fp32x2 a - b, round to nearest (sm_100+).
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
+// Packed fp32x2 a * b + c, all operands pairs, round to nearest (sm_100+).
+__device__ __forceinline__ float2 ffma2v(float2 a, float2 b, float2 c) {
+    float2 r;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+// 2^x for two values on the FMA and integer pipes, so that part of a softmax's
+// exponentials can bypass the special-function unit (which the softmax saturates).
+// Cody-Waite style reduction: x = n + f with n = rint(x) (the add of 1.5 * 2^23 rounds
+// to an integer and leaves n in the low mantissa bits), f in [-1/2, 1/2];
+// 2^f = 1 + f * (a0 + f * (a1 + f * a2)), the Chebyshev interpolant written out by
+// exp2_poly.py (relative error below 2.5e-4 over the range); n is then added into the
+// exponent field.  x is clamped below at -127, where f = 0 and the result is exactly
+// +0.0, so -inf (a masked score) maps to 0.  Valid for x <= 127.
+constexpr float kExp2A0 = 0x1.62e43p-1f;
+constexpr float kExp2A1 = 0x1.efb038p-3f;
+constexpr float kExp2A2 = 0x1.c8bdfap-5f;
+__device__ __forceinline__ float2 ex2_fma2(float2 x) {
+    constexpr float kMagic = 12582912.0f;
+    x.x = fmaxf(x.x, -127.0f);
+    x.y = fmaxf(x.y, -127.0f);
+    const float2 t = fadd2(x, make_float2(kMagic, kMagic));
+    const float2 f = fsub2(x, fsub2(t, make_float2(kMagic, kMagic)));
+    float2 u = ffma2v(make_float2(kExp2A2, kExp2A2), f, make_float2(kExp2A1, kExp2A1));
+    u = ffma2v(u, f, make_float2(kExp2A0, kExp2A0));
+    const float2 pw = ffma2v(u, f, make_float2(1.0f, 1.0f));
+    return make_float2(__uint_as_float(__float_as_uint(pw.x) + (__float_as_uint(t.x) << 23)),
+                       __uint_as_float(__float_as_uint(pw.y) + (__float_as_uint(t.y) << 23)));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -187,9 +187,19 @@ gqa_status gqa_get_device_status(gqa_stream_t stream);
  * device-side bounded waits that expired since the last call (0 where none): diag[0] the
  * first overall, diag[1..4] the first of each kernel role 0..3.  A code is
  * (kernel << 24) | (role << 20) | (barrier << 16) | (tile index & 0xffff), kernel 1 =
- * prefill d=128, 2 = prefill d=256/512, 3 = decode.  For diagnosing
- * GQA_ERR_DEVICE_TIMEOUT; gqa_get_device_status leaves the codes in place. */
+ * prefill d=128, 2 = prefill d=256/512, 3 = decode, 4 = gqa_watchdog_selftest.  For
+ * diagnosing GQA_ERR_DEVICE_TIMEOUT; gqa_get_device_status leaves the codes in place. */
 gqa_status gqa_get_device_diag(gqa_stream_t stream, int32_t *diag, int n);
+
+/* Self-test of the device-side watchdog (the pages have no counterpart: this checks the
+ * library's own failure detection).  Enqueues on `stream` one warp that waits on an
+ * mbarrier nothing ever arrives on, bounded by limit_ns nanoseconds, with the same wait
+ * and reporting code as the attention kernels.  The wait expires, the kernel records
+ * GQA_ERR_DEVICE_TIMEOUT and diagnostic code 4 << 24 and returns normally: the next
+ * gqa_get_device_status returns GQA_ERR_DEVICE_TIMEOUT and the context stays usable.
+ * limit_ns in [1000, 2000000000] (1 us .. 2 s, the kernels' own limit), else
+ * GQA_ERR_INVALID_ARG without launching. */
+gqa_status gqa_watchdog_selftest(int64_t limit_ns, gqa_stream_t stream);
 
 /* Static, human-readable text for a status code. */
 const char *gqa_status_string(int status);

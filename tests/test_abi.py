@@ -77,3 +77,10 @@ def test_bad_arguments_rejected_on_host():
     assert f(L.gqa_kv_append(None, 1, fake, fake, 1, 128, None, None)) == "GQA_ERR_INVALID_ARG"
     assert f(L.gqa_rope_apply(fake, fake, 1, 1, 4, 128, 10, fake, 12, None)) == "GQA_ERR_RANGE"
     assert gqa.gqa_status_string(-6) == "device-side wait timed out"
+
+
+def test_watchdog_selftest_limits_rejected_on_host():
+    L = gqa.lib()
+    S = gqa.STATUS_NAMES
+    for bad in (0, 999, -5, 2_000_000_001):
+        assert S[L.gqa_watchdog_selftest(bad, None)] == "GQA_ERR_INVALID_ARG", bad
