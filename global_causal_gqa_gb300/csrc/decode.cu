@@ -27,6 +27,7 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kWarps = 8;
+constexpr int kDecodeSmem = kWarps * 2 * 512 * 16;   // two 8 KB table stages per warp
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -51,8 +52,32 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
     return r;
 }
 
+// 16-byte asynchronous copy global -> shared, cached in L1 (the 8 warps of a CTA read
+// the same table rows).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint32_t word(const uint4 &u, int i) {
     return i == 0 ? u.x : i == 1 ? u.y : i == 2 ? u.z : u.w;
+}
+
+// Rotates the two pairs in 32-bit word q of chunks a and b by t = (cos0, sin0, cos1, sin1)
+// (amplitude included).
+__device__ __forceinline__ void rotate_word(uint4 &a, uint4 &b, int q, const float4 &t) {
+    uint32_t &aw = q == 0 ? a.x : q == 1 ? a.y : q == 2 ? a.z : a.w;
+    uint32_t &bw = q == 0 ? b.x : q == 1 ? b.y : q == 2 ? b.z : b.w;
+    const float a0 = bf16lo(aw), a1 = bf16hi(aw), b0 = bf16lo(bw), b1 = bf16hi(bw);
+    aw = pack_bf16x2(fmaf(a0, t.x, -b0 * t.y), fmaf(a1, t.z, -b1 * t.w));
+    bw = pack_bf16x2(fmaf(a0, t.y, b0 * t.x), fmaf(a1, t.w, b1 * t.z));
 }
 
 // Rotates the 8 pairs (a[e], b[e]) held in two 16-byte chunks by the table entries
@@ -152,6 +177,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m_run0 = -CUDART_INF_F, m_run1 = -CUDART_INF_F, l_run0 = 0.f, l_run1 = 0.f;
 
+    // This warp's two table stages: the 16 table rows of a key block, 16-byte entry
+    // (k, lane) at k * 32 + (lane ^ 2 (k & 3)) holding what lane (gq, tq) needs for
+    // k = 8 rs + 4 c + qq: pairs 32c + 8tq + 2qq and the next one at position kb + gq + 8 rs.
+    // The XOR keeps both the copies in and the reads out free of bank conflicts.
+    extern __shared__ float4 dsmem[];
+    float4 *stage_base = dsmem + (size_t)warp * 2 * 512;
+
     const __nv_bfloat16 *kbase = static_cast<const __nv_bfloat16 *>(desc.k) + (size_t)g * sv.cap * kD;
     const __nv_bfloat16 *vbase = static_cast<const __nv_bfloat16 *>(desc.v) + (size_t)g * sv.cap * kD;
     auto slot_of = [&](int key) {
@@ -159,9 +191,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         return s >= sv.cap ? s - sv.cap : s;
     };
 
-    // One block = 16 keys: K rows kb + gq and kb + gq + 8, V rows kb + 2tq + {0, 1, 8, 9};
-    // rows at or past k_end are clamped in range and get weight 0.  Two register buffers:
-    // the next block's loads are in flight while the current block is computed.
+    // One block = 16 keys: K rows kb + gq and kb + gq + 8, V rows kb + 2tq + {0, 1, 8, 9}
+    // (16-byte chunks gq and 8 + gq of each, so every load instruction reads whole
+    // 128-byte lines), and the block's table rows copied to shared memory; rows at or
+    // past k_end are clamped in range and get weight 0.  Two register buffers and two
+    // table stages: the next block's loads are in flight while the current block is
+    // computed.
     struct Block {
         uint4 k0[4], k1[4], vv[4][2];
         int kb;
@@ -180,20 +215,43 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         for (int i = 0; i < 4; ++i) {
             const int key = min(kb + 2 * tq + (i & 1) + ((i >> 1) << 3), k_end - 1);
             const uint4 *vr = reinterpret_cast<const uint4 *>(vbase + (size_t)slot_of(key) * kD);
-            bl.vv[i][0] = ld_stream(vr + 2 * gq);
-            bl.vv[i][1] = ld_stream(vr + 2 * gq + 1);
+            bl.vv[i][0] = ld_stream(vr + gq);
+            bl.vv[i][1] = ld_stream(vr + 8 + gq);
         }
+        // table rows kb .. kb + 15: instruction i copies row i (clamped), lane = 16-byte
+        // piece of the row, i.e. pairs 2 lane, 2 lane + 1 = 32c + 8tq + 2qq
+        __syncwarp();   // every lane is done reading this stage's previous block
+        float4 *stg = stage_base + (((kb - k_start) >> 4) & 1) * 512;
+        const int kq = ((lane >> 4) << 2) | (lane & 3);   // 4c + qq
+        const int lp_lo = (lane >> 2) & 3;                  // tq
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int row = min(kb + i, k_end - 1);
+            const int k = ((i >> 3) << 3) | kq;
+            const int lp = ((i & 7) << 2) | lp_lo;
+            cp_async16(stg + k * 32 + (lp ^ ((k & 3) << 1)),
+                       reinterpret_cast<const float4 *>(table + (size_t)row * (kD / 2)) + lane);
+        }
+        cp_async_commit();
     };
-    auto compute = [&](Block &bl) {
+    auto compute = [&](Block &bl, bool next_pending) {
         const int kb = bl.kb;
         const int key0 = kb + gq, key1 = kb + gq + 8;
         const bool ok0 = key0 < k_end, ok1 = key1 < k_end;
-        const int kk0 = ok0 ? key0 : k_end - 1, kk1 = ok1 ? key1 : k_end - 1;
-        // rotate K at logical positions kk0, kk1
+        // this block's table stage has landed (the next block's copies may still run)
+        if (next_pending) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        __syncwarp();
+        const float4 *stg = stage_base + (((kb - k_start) >> 4) & 1) * 512;
+        // rotate K at logical positions kb + gq, kb + gq + 8 (clamped rows: k_end - 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-            rotate8(bl.k0[c], bl.k0[c + 2], table + (size_t)kk0 * (kD / 2) + 32 * c + 8 * tq);
-            rotate8(bl.k1[c], bl.k1[c + 2], table + (size_t)kk1 * (kD / 2) + 32 * c + 8 * tq);
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const int sw = lane ^ (qq << 1);
+                rotate_word(bl.k0[c], bl.k0[c + 2], qq, stg[(4 * c + qq) * 32 + sw]);
+                rotate_word(bl.k1[c], bl.k1[c + 2], qq, stg[(8 + 4 * c + qq) * 32 + sw]);
+            }
         }
         // S^T (16 keys x 8 heads) in two independent accumulation chains
         float s[4] = {0.f, 0.f, 0.f, 0.f}, t[4] = {0.f, 0.f, 0.f, 0.f};
@@ -227,7 +285,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         const uint32_t pb0 = transpose8x8(pack_bf16x2(p0, p1));
         const uint32_t pb1 = transpose8x8(pack_bf16x2(p2, p3));
         // O^T (128 dims x 8 heads) += V^T P^T; dims permuted: row g of m-tile mt is
-        // dim 16g + 2mt, row g + 8 is dim 16g + 2mt + 1.
+        // dim 64 (mt >> 2) + 8g + 2 (mt & 3), row g + 8 is the dim after it.
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
             o[mt][0] *= f0;
@@ -244,11 +302,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     Block ba, bb;
     load(ba, k_start);
     for (int kb = k_start; kb < k_end; kb += 32) {
-        if (kb + 16 < k_end) load(bb, kb + 16);
-        compute(ba);
-        if (kb + 16 >= k_end) break;
-        if (kb + 32 < k_end) load(ba, kb + 32);
-        compute(bb);
+        const bool more1 = kb + 16 < k_end;
+        if (more1) load(bb, kb + 16);
+        compute(ba, more1);
+        if (!more1) break;
+        const bool more2 = kb + 32 < k_end;
+        if (more2) load(ba, kb + 32);
+        compute(bb, more2);
     }
 
     // partial sums of l over the 8 key rows held across gq
@@ -265,20 +325,20 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             ws_ml[2 * rec0] = m_run0;
             ws_ml[2 * rec0 + 1] = l_run0;
         }
-        float4 *dst = reinterpret_cast<float4 *>(ws_o + rec0 * kD + 16 * gq);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            dst[i] = make_float4(o[2 * i][0], o[2 * i][2], o[2 * i + 1][0], o[2 * i + 1][2]);
+            reinterpret_cast<float4 *>(ws_o + rec0 * kD + 64 * (i >> 1) + 8 * gq)[i & 1] =
+                make_float4(o[2 * i][0], o[2 * i][2], o[2 * i + 1][0], o[2 * i + 1][2]);
     }
     if (h1 < G) {
         if (gq == 0) {
             ws_ml[2 * rec1] = m_run1;
             ws_ml[2 * rec1 + 1] = l_run1;
         }
-        float4 *dst = reinterpret_cast<float4 *>(ws_o + rec1 * kD + 16 * gq);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            dst[i] = make_float4(o[2 * i][1], o[2 * i][3], o[2 * i + 1][1], o[2 * i + 1][3]);
+            reinterpret_cast<float4 *>(ws_o + rec1 * kD + 64 * (i >> 1) + 8 * gq)[i & 1] =
+                make_float4(o[2 * i][1], o[2 * i][3], o[2 * i + 1][1], o[2 * i + 1][3]);
     }
 }
 
@@ -319,7 +379,14 @@ cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int
     const int warps = Hkv < kWarps ? Hkv : kWarps;
     dim3 grid(nsplit, nseq, (Hkv + kWarps - 1) / kWarps);
     const float scale_log2 = scale * 1.4426950408889634f;
-    decode_partial_kernel<<<grid, warps * 32, 0, s>>>(
+    static bool attr_done = false;
+    if (!attr_done) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            decode_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    decode_partial_kernel<<<grid, warps * 32, warps * 2 * 512 * sizeof(float4), s>>>(
         static_cast<const __nv_bfloat16 *>(q), descs, Hq, Hkv, scale_log2, max_len, nsplit,
         ws_ml, ws_o, status);
     cudaError_t e = cudaGetLastError();

@@ -25,7 +25,10 @@ cudaError_t launch_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new,
                              int *status, cudaStream_t s);
 
 // Decode (decode.cu)
-constexpr int kDecodeChunk = 1024;  // keys per split
+#ifndef GQA_DECODE_CHUNK
+#define GQA_DECODE_CHUNK 1024
+#endif
+constexpr int kDecodeChunk = GQA_DECODE_CHUNK;  // keys per split
 int decode_num_splits(int max_len);
 cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
                           int d, float scale, int max_len, void *o, float *lse,
