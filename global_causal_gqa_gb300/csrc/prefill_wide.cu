@@ -7,16 +7,18 @@
 // a 128 x d fp32 output tile alone takes d of the 512 TMEM columns.
 //
 // CTA = (batch, query head, 128-row query block, output slice).  One query tile per CTA;
-// its score tile S is double-buffered in TMEM so that S(j+1) = Q K(j+1)^T runs on the
-// tensor core while the softmax warps work on S(j).  TMEM: S_a, S_b (BN columns each) and
-// O (DV columns).  K streams through a ring of 128-dim chunks (TMA, 128-byte swizzle), V
-// (only the DV output columns of this CTA) through its own ring.
-//   d = 256: BN = 128, DV = 256: 128 + 128 + 256 = 512 columns.
-//   d = 512: BN = 64, DV = 256, two output slices per query tile: both CTAs of a pair
-//            compute the full S (the score contraction runs over all 512 dims) and each
-//            accumulates half of O -- 64 + 64 + 256 = 384 columns.
-// Warps: 0 TMA producer of Q and K, 1 TMEM owner + MMA issuer, 2 TMA producer of V,
-// 3 idle, 4-7 softmax/epilogue (one thread per query row).  Q is rotated (RoPE) in shared memory after it lands; pairs
+// its score tile S (128 keys) is double-buffered in TMEM so that S(j+2) = Q K(j+2)^T can
+// run on the tensor core while the softmax warps work on S(j+1).  TMEM: S_a, S_b (128
+// columns each) and O (the CTA's 256 output columns).  K (128-dim chunks of a key tile)
+// and V (128-dim halves of the CTA's output columns) stream through one ring of 32 KB
+// slots, loaded by TMA (128-byte swizzle) in exactly the order the MMA thread uses them:
+// K(0), K(1), then V(j), K(j + 2) for j = 0, 1, ...
+//   d = 256: one output slice; Q 64 KB + 5 ring slots.
+//   d = 512: two output slices per query tile: both CTAs of a pair compute the full S
+//            (the score contraction runs over all 512 dims) and each accumulates half of
+//            O; Q 128 KB + 3 ring slots.
+// Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2-3 idle, 4-7 softmax/epilogue (one
+// thread per query row).  Q is rotated (RoPE) in shared memory after it lands; pairs
 // (j, j + d/2) sit at the same offset of boxes k and k + d/128.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -39,17 +41,18 @@ struct Wide;
 
 template <>
 struct Wide<256> {
-    static constexpr int BN = 128, DV = 256, KST = 2, VST = 1;
+    static constexpr int BN = 128, DV = 256, NS = 5;
 };
 template <>
 struct Wide<512> {
-    static constexpr int BN = 64, DV = 256, KST = 4, VST = 1;
+    static constexpr int BN = 128, DV = 256, NS = 3;
 };
+constexpr int kSlotBytes = 128 * 256;   // 128 rows x 128 bf16 (two 64-column TMA boxes)
+constexpr int kMaxSlots = 5;
 
 struct WBars {
     uint64_t q_full, q_ready;
-    uint64_t k_full[4], k_empty[4];
-    uint64_t v_full[2], v_empty[2];
+    uint64_t full[kMaxSlots], empty[kMaxSlots];
     uint64_t s_full[2], p_full[2], o_done, mma_done;
     // the last PV product: S(j+2) waits only for PV(j), so when the softmax finishes the
     // last tile PV(n-2) may still run and o_done can be two phases behind -- its parity
@@ -57,7 +60,6 @@ struct WBars {
     uint64_t o_final;
     uint32_t tmem_base;
 };
-
 static_assert(sizeof(WBars) <= 256, "barrier block");
 
 struct WParams {
@@ -79,17 +81,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const WParams p) {
-    constexpr int BN = Wide<D>::BN, DV = Wide<D>::DV, KST = Wide<D>::KST, VST = Wide<D>::VST;
+    constexpr int BN = Wide<D>::BN, DV = Wide<D>::DV, NS = Wide<D>::NS;
     constexpr int NKC = D / 128;                  // 128-dim K chunks per key tile
+    constexpr int NVH = DV / 128;                 // 128-dim V halves per key tile
     constexpr int QBOX = kBM * 128;               // 128 rows x 64 bf16
     constexpr int QBYTES = (D / 64) * QBOX;
-    constexpr int KBOX = BN * 128;                // BN rows x 64 bf16
-    constexpr int KCHUNK = 2 * KBOX;              // BN rows x 128 bf16
-    constexpr int VTILE = (DV / 64) * KBOX;       // BN rows x DV bf16
-    constexpr int OFF_K = QBYTES;
-    constexpr int OFF_V = OFF_K + KST * KCHUNK;
-    constexpr int OFF_BAR = OFF_V + VST * VTILE;
+    constexpr int BOX = BN * 128;                 // BN rows x 64 bf16
+    constexpr int OFF_RING = QBYTES;
+    constexpr int OFF_BAR = OFF_RING + NS * kSlotBytes;
     constexpr uint32_t TS0 = 0, TS1 = BN, TO = 2 * BN;
+    static_assert(BN == 128 && 2 * BOX == kSlotBytes && NS <= kMaxSlots, "ring layout");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -114,13 +115,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
         mbar_init(&bars->q_ready, 128);
-        for (int i = 0; i < KST; ++i) {
-            mbar_init(&bars->k_full[i], 1);
-            mbar_init(&bars->k_empty[i], 1);
-        }
-        for (int i = 0; i < VST; ++i) {
-            mbar_init(&bars->v_full[i], 1);
-            mbar_init(&bars->v_empty[i], 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&bars->full[i], 1);
+            mbar_init(&bars->empty[i], 1);
         }
         mbar_init(&bars->s_full[0], 1);
         mbar_init(&bars->s_full[1], 1);
@@ -140,104 +137,97 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
+    // The ring sequence, shared by the producer and the MMA thread: K(0), K(1), then for
+    // j = 0 .. n-1: V(j), and K(j + 2) if it exists; each K is NKC slots, each V is NVH.
     if (warp == 0) {
-        // ================= TMA producer: Q, then K chunks =================
+        // ================= TMA producer: Q, then the ring =================
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
             const int zq = b * p.Hq + h, zk = b * p.Hkv + g;
             mbar_arrive_expect_tx(&bars->q_full, QBYTES);
             for (int i = 0; i < D / 64; ++i)
                 tma_load_3d(sQ + i * QBOX, &tmQ, &bars->q_full, 64 * i, mb * kBM, zq);
             bool ok = true;
-            int issued = 0;
-            for (int u = 0; u < n_tiles * NKC && ok; ++u) {
-                const int j = u / NKC, c = u % NKC, st = u % KST;
-                if (u >= KST && !(ok = mbar_wait(&bars->k_empty[st], ((u / KST) - 1) & 1))) {
+            int u = 0;
+            // one 32 KB slot: rows n0 .. n0 + 127, columns c0 .. c0 + 127 of K or V
+            auto put = [&](const CUtensorMap *map, int n0, int c0) {
+                const int st = u % NS;
+                if (u >= NS && !(ok = mbar_wait(&bars->empty[st], ((u / NS) - 1) & 1))) {
                     set_timeout(p.status, kDiagPrefillWide, 0, 1, u);
-                    break;
+                    return;
                 }
-                const int n0 = (kt_first + j) * BN;
-                uint8_t *dst = smem + OFF_K + st * KCHUNK;
-                mbar_arrive_expect_tx(&bars->k_full[st], KCHUNK);
-                tma_load_3d(dst, &tmK, &bars->k_full[st], 128 * c, n0, zk);
-                tma_load_3d(dst + KBOX, &tmK, &bars->k_full[st], 128 * c + 64, n0, zk);
-                issued = u + 1;
+                uint8_t *dst = smem + OFF_RING + st * kSlotBytes;
+                mbar_arrive_expect_tx(&bars->full[st], kSlotBytes);
+                tma_load_3d(dst, map, &bars->full[st], c0, n0, zk);
+                tma_load_3d(dst + BOX, map, &bars->full[st], c0 + 64, n0, zk);
+                ++u;
+            };
+            auto put_k = [&](int j) {
+                for (int c = 0; c < NKC && ok; ++c) put(&tmK, (kt_first + j) * BN, 128 * c);
+            };
+            auto put_v = [&](int j) {
+                for (int hh = 0; hh < NVH && ok; ++hh)
+                    put(&tmV, (kt_first + j) * BN, slice * DV + 128 * hh);
+            };
+            put_k(0);
+            if (n_tiles > 1) put_k(1);
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                put_v(j);
+                if (j + 2 < n_tiles) put_k(j + 2);
             }
             if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
             // never leave the CTA with copies in flight
             mbar_wait(&bars->q_full, 0);
-            for (int u = max(0, issued - KST); u < issued; ++u)
-                mbar_wait(&bars->k_full[u % KST], (u / KST) & 1);
-        }
-        __syncwarp();
-    } else if (warp == 2) {
-        // ================= TMA producer: V (this CTA's output columns) =================
-        if (lane == 0) {
-            tma_prefetch_desc(&tmV);
-            const int zk = b * p.Hkv + g;
-            bool ok = true;
-            int issued = 0;
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int vs = j % VST;
-                if (j >= VST && !(ok = mbar_wait(&bars->v_empty[vs], ((j / VST) - 1) & 1))) {
-                    set_timeout(p.status, kDiagPrefillWide, 2, 3, j);
-                    break;
-                }
-                const int n0 = (kt_first + j) * BN;
-                uint8_t *dst = smem + OFF_V + vs * VTILE;
-                mbar_arrive_expect_tx(&bars->v_full[vs], VTILE);
-                for (int i = 0; i < DV / 64; ++i)
-                    tma_load_3d(dst + i * KBOX, &tmV, &bars->v_full[vs], slice * DV + 64 * i, n0,
-                                zk);
-                issued = j + 1;
-            }
-            if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
-            for (int j = max(0, issued - VST); j < issued; ++j)
-                mbar_wait(&bars->v_full[j % VST], (j / VST) & 1);
+            for (int w = max(0, u - NS); w < u; ++w) mbar_wait(&bars->full[w % NS], (w / NS) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kBM, BN, 0, 0);
-            const uint32_t idesc_o = idesc_bf16_f32(kBM, DV, 0, 1);
+            const uint32_t idesc_o = idesc_bf16_f32(kBM, 128, 0, 1);
             const uint32_t qaddr = smem_u32(sQ);
-            const uint32_t kaddr = smem_u32(smem + OFF_K), vaddr = smem_u32(smem + OFF_V);
+            const uint32_t ring = smem_u32(smem + OFF_RING);
             bool ok = mbar_wait(&bars->q_ready, 0);
             if (!ok) set_timeout(p.status, kDiagPrefillWide, 1, 4, 0);
             tc_fence_after();
+            int u = 0;
+            // waits for the next ring slot; returns its shared-memory address
+            auto take = [&](uint32_t &addr) {
+                const int st = u % NS;
+                if (!(ok = mbar_wait(&bars->full[st], (u / NS) & 1))) {
+                    set_timeout(p.status, kDiagPrefillWide, 1, 0, u);
+                    return -1;
+                }
+                tc_fence_after();
+                addr = ring + st * kSlotBytes;
+                return st;
+            };
             auto issue_s = [&](int j) {
                 const uint32_t dst = tmem + ((j & 1) ? TS1 : TS0);
                 for (int c = 0; c < NKC && ok; ++c) {
-                    const int u = j * NKC + c, st = u % KST;
-                    if (!(ok = mbar_wait(&bars->k_full[st], (u / KST) & 1))) {
-                        set_timeout(p.status, kDiagPrefillWide, 1, 0, u);
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t ka = kaddr + st * KCHUNK;
+                    uint32_t ka;
+                    const int st = take(ka);
+                    if (st < 0) break;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const int dk = 8 * c + kk;   // 16-dim step over the whole head
                         const uint64_t ad = sdesc_sw128(
                             qaddr + (dk >> 2) * QBOX + (dk & 3) * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(
-                            ka + (kk >> 2) * KBOX + (kk & 3) * 32, 16, 1024);
+                            ka + (kk >> 2) * BOX + (kk & 3) * 32, 16, 1024);
                         umma_ss(dst, ad, bd, idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(&bars->k_empty[st]);
+                    umma_commit(&bars->empty[st]);
+                    ++u;
                 }
                 if (ok) umma_commit(&bars->s_full[j & 1]);
             };
             if (ok) issue_s(0);
             if (ok && n_tiles > 1) issue_s(1);
             for (int j = 0; j < n_tiles && ok; ++j) {
-                const int vs = j % VST;
-                if (!(ok = mbar_wait(&bars->v_full[vs], (j / VST) & 1))) {
-                    set_timeout(p.status, kDiagPrefillWide, 1, 2, j);
-                    break;
-                }
                 // one barrier per S buffer: the softmax may finish S(j+1) before this wait,
                 // never S(j+2) (issued below, after PV(j)), so no phase is skipped
                 if (!(ok = mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1))) {
@@ -246,14 +236,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t pcol = tmem + ((j & 1) ? TS1 : TS0);
-                const uint32_t va = vaddr + vs * VTILE;
+                for (int hh = 0; hh < NVH && ok; ++hh) {
+                    uint32_t va;
+                    const int st = take(va);
+                    if (st < 0) break;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    umma_ts(tmem + TO, pcol + kk * 8, sdesc_sw128(va + kk * 2048, KBOX, 1024),
-                            idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        umma_ts(tmem + TO + 128 * hh, pcol + kk * 8,
+                                sdesc_sw128(va + kk * 2048, BOX, 1024), idesc_o,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&bars->empty[st]);
+                    ++u;
+                }
+                if (!ok) break;
                 umma_commit(&bars->o_done);
                 if (j == n_tiles - 1) umma_commit(&bars->o_final);
-                umma_commit(&bars->v_empty[vs]);
                 // S(j+2) reuses the TMEM buffer P(j) sits in: PV(j) must have finished
                 // reading P(j) before the first S(j+2) product is written there
                 if (j + 2 < n_tiles) {
@@ -448,8 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 constexpr int wide_smem_bytes() {
-    return (D / 64) * kBM * 128 + Wide<D>::KST * 2 * Wide<D>::BN * 128 +
-           Wide<D>::VST * (Wide<D>::DV / 64) * Wide<D>::BN * 128 + 256 + 1024;
+    return (D / 64) * kBM * 128 + Wide<D>::NS * kSlotBytes + 256 + 1024;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
