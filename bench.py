@@ -59,19 +59,24 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def traffic_record(kernel: str, source: str):
-    """DRAM bytes per launch from a committed ncu capture, valid only while the kernel
-    source is byte-identical to the one profiled."""
+def traffic_record(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from a committed ncu capture
+    (profiles/traffic.json), valid only while the kernel source is byte-identical to the
+    one profiled; None otherwise."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        rec = json.load(f).get(kernel)
+        rec = json.load(f).get(kernel, {}).get(workload)
     if not rec:
         return None
-    with open(os.path.join(ROOT, "global_causal_gqa_gb300", "csrc", source), "rb") as f:
+    with open(os.path.join(ROOT, "global_causal_gqa_gb300", "csrc", rec["source"]), "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()
     return rec["bytes_per_launch"] if rec.get("source_sha256") == sha else None
+
+
+def kernel_name(d: int) -> str:
+    return "prefill_kernel" if d == 128 else f"prefill_wide_kernel<{d}>"
 
 
 class ClockSampler:
@@ -223,7 +228,7 @@ def prefill_setup(layer):
     return st
 
 
-def bench_prefill(layers, steps: int, warmup: int, stream, peaks, peak_src, world,
+def bench_prefill(name, layers, steps: int, warmup: int, stream, peaks, peak_src, world,
                   with_e2e: bool, clocks_index=None):
     """One step = every layer of the workload in sequence, each = K rotated once
     (gqa_rope_apply) + the attention kernel (gqa_attn_prefill, k_is_rotated=1)."""
@@ -273,25 +278,31 @@ def bench_prefill(layers, steps: int, warmup: int, stream, peaks, peak_src, worl
     step_ms_max = max_over_ranks(world, step_ms)
     value = world * flops / (step_ms_max * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    achieved = flops / (kern_ms * 1e-3) / 1e12
+    # roofline of the dominant kernel: the layer with the largest device time
+    dom = max(range(len(layers)), key=lambda i: per_layer[i])
+    Ld = layers[dom]
+    dom_flops = acc.prefill_flops(Ld.B, Ld.Hq, Ld.T, Ld.S, Ld.d, Ld.window)
+    achieved = dom_flops / (per_layer[dom] * 1e-3) / 1e12
+    dom_wl = name if len(layers) == 1 else f"{name}[layer {dom}]"
     out = {
         "value": value, "unit": "TFLOP/s", "ms_per_step": step_ms_max,
         "kernel_ms": {"rope_k": rope_ms, "prefill": kern_ms},
         "flops_per_step": flops, "wall_s": wall,
-        "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved,
+        "roofline": {"bound": "tensor", "kernel": kernel_name(Ld.d), "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"bf16_tflops (burst, {peak_src})",
-                     "traffic": traffic_record("prefill_kernel", "prefill.cu")},
+                     "traffic": traffic_record(kernel_name(Ld.d), dom_wl)},
         "gpu_launches": 2 * len(layers) * steps,
         "clocks": sampler.summary() if sampler else None,
     }
     if len(layers) > 1:
+        out["roofline"]["layer"] = dom
+        all_tf = flops / (kern_ms * 1e-3) / 1e12
+        out["roofline"]["all_attention_kernels"] = {"achieved": all_tf, "frac": all_tf / peak}
         out["per_layer"] = [
-            {"d": L.d, "window": L.window, "ms": ms,
+            {"d": L.d, "window": L.window, "kernel": kernel_name(L.d), "ms": ms,
              "tflops": acc.prefill_flops(L.B, L.Hq, L.T, L.S, L.d, L.window) / (ms * 1e-3) / 1e12}
             for L, ms in zip(layers, per_layer)]
-        out["roofline"]["kernel"] = "prefill_kernel / prefill_wide_kernel"
-        out["roofline"]["traffic"] = None
     if with_e2e:
         out["e2e"] = e2e_prefill(layers[0], sts[0], steps, warmup, stream,
                                  acc.prefill_flops(layers[0].B, layers[0].Hq, layers[0].T,
@@ -410,7 +421,7 @@ def bench_decode(w, steps, warmup, stream, peaks, peak_src, world, with_e2e, clo
         "roofline": {"bound": "hbm", "kernel": "decode_partial_kernel + decode_combine_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"hbm_gbs ({peak_src})",
-                     "traffic": traffic_record("decode_partial_kernel", "decode.cu")},
+                     "traffic": traffic_record("decode_partial_kernel", w.name)},
         "gpu_launches": 3 * steps,
         "clocks": sampler.summary() if sampler else None,
     }
@@ -577,10 +588,15 @@ def config_of(wl):
                 "global_len": list(wl.global_len_range), "window": wl.window,
                 "l2": "flushed before every timed step (256 MiB write)"}
     L = wl.layers[0]
-    return {"workload": wl.name, "layers": len(wl.layers), "B": L.B, "T": L.T, "S": L.S,
-            "Hq": L.Hq, "Hkv": L.Hkv, "d": L.d, "window": L.window,
-            "rope_base": L.rope.base, "yarn_factor": L.rope.yarn_factor,
-            "l2": "flushed before every timed step (256 MiB write)"}
+    cfg = {"workload": wl.name, "layers": len(wl.layers), "B": L.B, "T": L.T, "S": L.S,
+           "Hq": L.Hq, "Hkv": L.Hkv, "d": L.d, "window": L.window,
+           "rope_base": L.rope.base, "yarn_factor": L.rope.yarn_factor,
+           "l2": "flushed before every timed step (256 MiB write)"}
+    if len(wl.layers) > 1:
+        cfg["layer_shapes"] = [{"d": x.d, "Hq": x.Hq, "Hkv": x.Hkv, "window": x.window,
+                                "rope_base": x.rope.base,
+                                "rotate_fraction": x.rope.rotate_fraction} for x in wl.layers]
+    return cfg
 
 
 # ----------------------------------------------------------------------------------------
@@ -594,11 +610,18 @@ def main():
     ap.add_argument("--impl", choices=["gqa", "reference"], default="gqa")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layer", type=int, default=None,
+                    help="time only this layer of a multi-layer prefill workload (profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
     from workloads import DecodeWorkload, get_workload
     wl = get_workload(args.workload)
+    if args.layer is not None:
+        import dataclasses
+        wl = dataclasses.replace(wl, name=f"{wl.name}[layer {args.layer}]",
+                                 layers=(wl.layers[args.layer],))
+        args.no_extra = True
     world, rank, local = dist_setup(args)
 
     if args.impl == "reference":
@@ -618,8 +641,8 @@ def main():
         main_res = bench_decode(wl, args.steps, args.warmup, stream, peaks, peak_src, world,
                                 True, clock_idx)
     else:
-        main_res = bench_prefill(list(wl.layers), args.steps, args.warmup, stream, peaks,
-                                 peak_src, world, True, clock_idx)
+        main_res = bench_prefill(wl.name, list(wl.layers), args.steps, args.warmup, stream,
+                                 peaks, peak_src, world, True, clock_idx)
 
     extra = []
     if world == 1 and not args.no_extra:
@@ -632,7 +655,8 @@ def main():
             if isinstance(other, DecodeWorkload):
                 r = bench_decode(other, ks, kw, stream, peaks, peak_src, 1, False)
             else:
-                r = bench_prefill(list(other.layers), ks, kw, stream, peaks, peak_src, 1, False)
+                r = bench_prefill(name, list(other.layers), ks, kw, stream, peaks, peak_src, 1,
+                                  False)
             r.pop("clocks", None)
             extra.append({"workload": name, "steps": ks, "warmup": kw, **r})
 
@@ -653,6 +677,8 @@ def main():
             "gpu_launches": main_res["gpu_launches"], "clocks": main_res["clocks"],
             "kernel_ms": main_res["kernel_ms"], "extra": extra,
         }
+        if "per_layer" in main_res:
+            line["per_layer"] = main_res["per_layer"]
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
