@@ -75,8 +75,11 @@ def traffic_record(kernel: str, workload: str):
     return rec["bytes_per_launch"] if rec.get("source_sha256") == sha else None
 
 
-def kernel_name(d: int) -> str:
-    return "prefill_kernel" if d == 128 else f"prefill_wide_kernel<{d}>"
+def kernel_name(L) -> str:
+    from global_causal_gqa_gb300 import accounting as acc
+    if L.d == 128:
+        return acc.prefill_d128_kernel(L.T, L.S, L.window)
+    return f"prefill_wide_kernel<{L.d}>"
 
 
 class ClockSampler:
@@ -288,10 +291,10 @@ def bench_prefill(name, layers, steps: int, warmup: int, stream, peaks, peak_src
         "value": value, "unit": "TFLOP/s", "ms_per_step": step_ms_max,
         "kernel_ms": {"rope_k": rope_ms, "prefill": kern_ms},
         "flops_per_step": flops, "wall_s": wall,
-        "roofline": {"bound": "tensor", "kernel": kernel_name(Ld.d), "achieved": achieved,
+        "roofline": {"bound": "tensor", "kernel": kernel_name(Ld), "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"bf16_tflops (burst, {peak_src})",
-                     "traffic": traffic_record(kernel_name(Ld.d), dom_wl)},
+                     "traffic": traffic_record(kernel_name(Ld), dom_wl)},
         "gpu_launches": 2 * len(layers) * steps,
         "clocks": sampler.summary() if sampler else None,
     }
@@ -300,7 +303,7 @@ def bench_prefill(name, layers, steps: int, warmup: int, stream, peaks, peak_src
         all_tf = flops / (kern_ms * 1e-3) / 1e12
         out["roofline"]["all_attention_kernels"] = {"achieved": all_tf, "frac": all_tf / peak}
         out["per_layer"] = [
-            {"d": L.d, "window": L.window, "kernel": kernel_name(L.d), "ms": ms,
+            {"d": L.d, "window": L.window, "kernel": kernel_name(L), "ms": ms,
              "tflops": acc.prefill_flops(L.B, L.Hq, L.T, L.S, L.d, L.window) / (ms * 1e-3) / 1e12}
             for L, ms in zip(layers, per_layer)]
     if with_e2e:

@@ -55,3 +55,18 @@ def kv_capacity_bytes(layers, N: int, elem_bytes: int = 2) -> int:
         tokens = N if w <= 0 else min(N, w)
         total += 2 * elem_bytes * n * hkv * d * tokens
     return total
+
+
+def prefill_d128_kernel(T: int, S: int, window: int) -> str:
+    """Which d = 128 prefill kernel the library launches for these positions: the
+    one-CTA-per-item kernel when the 128-row query blocks average at least 48 key tiles
+    (long causal sweeps), the persistent kernel otherwise.  Mirrors the rule in the
+    library's launcher; used to label measurements."""
+    n_mb = -(-T // 128)
+    tiles = 0
+    for mb in range(n_mb):
+        q_lo = S - T + mb * 128
+        q_hi = min(q_lo + 127, S - 1)
+        kt0 = max(0, q_lo - window + 1) // 128 if window > 0 else 0
+        tiles += q_hi // 128 - kt0 + 1
+    return "prefill_kernel" if tiles >= 48 * n_mb else "prefill_persistent_kernel"

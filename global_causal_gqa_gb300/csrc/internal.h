@@ -34,10 +34,16 @@ cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int
                           int d, float scale, int max_len, void *o, float *lse,
                           float *ws, int *status, cudaStream_t s);
 
-// Prefill (prefill.cu); returns a gqa_status
+// d = 128 prefill: picks the persistent kernel (prefill.cu) or the one-CTA-per-item
+// kernel (prefill_stream.cu) by the mean item length; returns a gqa_status
 int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, float *lse,
                    int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
                    const float *table, int table_len, int *status, cudaStream_t s);
+
+// d = 128 prefill, one CTA per work item (prefill_stream.cu); returns a gqa_status
+int launch_prefill_stream(const void *q, const void *k_rot, const void *v, void *o, float *lse,
+                          int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
+                          const float *table, int *status, cudaStream_t s);
 
 // Prefill for d = 256 / 512 (prefill_wide.cu); returns a gqa_status
 int launch_prefill_wide(const void *q, const void *k_rot, const void *v, void *o, float *lse,

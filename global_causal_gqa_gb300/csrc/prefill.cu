@@ -6,28 +6,42 @@
 // on the tensor cores with fp32 accumulators in tensor memory, and the softmax is an
 // online (running max / running sum) fp32 pass over each S tile.
 //
-// CTA = (batch b, KV head g, pair of query heads of that group, block of 128 query rows).
-// Both query tiles of a CTA sit at the same positions and read the same KV head, so they
-// share every K and V tile load and the same mask.  Only key tiles that intersect
-// [q_pos - W + 1, q_pos] for some row of the block are loaded (window tile skipping,
-// §1 and §5.3: local prefill costs O(T W)); the per-element mask is applied on the tiles
-// that straddle the diagonal or the window's lower edge only.
+// Work item = (batch b, KV head g, pair of query heads of that group, block of 128 query
+// rows).  Both query tiles of an item sit at the same positions and read the same KV
+// head, so they share every K and V tile load and the same mask.  Only key tiles that
+// intersect [q_pos - W + 1, q_pos] for some row of the block are loaded (window tile
+// skipping, §1 and §5.3: local prefill costs O(T W)); the per-element mask is applied on
+// the tiles that straddle the diagonal or the window's lower edge only.
 //
-// Warp roles (12 warps, 3 warpgroups):
-//   warp 0      TMA producer: Q tiles once, then K/V tiles into a 2-stage ring.
+// The kernel is persistent: one CTA per SM walks a list of items (snake order over
+// rounds, so a CTA that drew long causal rows in one round draws short ones in the
+// next).  The per-item fixed work overlaps the previous item: the next item's Q tiles
+// are loaded into the second of two Q buffers and rotated while the current item runs,
+// and the current item's epilogue overlaps the next item's first score products.
+//
+// Warp roles (12 warps, 3 warpgroups; 3 warps per SM sub-partition cap every thread at
+// 168 registers):
+//   warp 0      TMA producer: Q tiles of each item into Q buffer (item & 1), K and V
+//               tiles into a 3-slot ring in the order the MMA thread consumes them:
+//               K(0), V(0), K(1), V(1), ...
 //   warp 1      tensor-memory allocator and the single MMA-issuing thread.
-//   warps 2-3   idle (with 12 warps, 3 per SM sub-partition, every thread gets 168
-//               registers; fewer warps would not raise that cap).
-//   warps 4-7   softmax for query tile 0, warps 8-11 for query tile 1: one thread per
-//               query row; warp w reads TMEM lanes 32*(w%4).. (its lane quarter).
-// Q is rotated (RoPE, §6.1) in shared memory by the softmax warps right after it lands;
+//   warps 2-3   RoPE (§6.1) on each item's Q tiles in shared memory, ahead of use.
+//   warps 4-7   softmax + epilogue for query tile 0, warps 8-11 for query tile 1: one
+//               thread per query row; warp w reads TMEM lanes 32*(w%4).. (its quarter).
 // K arrives already rotated (the caller-side pass rotates each key once).
 //
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
 // P (bf16) overwrites the first 64 columns of its S tile and feeds the PV product
-// directly from tensor memory.  Rescaling of O is lazy: it happens only when a row's
-// maximum grows by more than 2^8, otherwise the stale maximum is kept (exact, since O
-// and the running sum always share one reference maximum).
+// directly from tensor memory.  The tensor pipe does not order an MMA's reads of its
+// TMEM operand before a later MMA's writes to the same columns, so S_i(j+1) is issued
+// only after PV_i(j) has completed.  Rescaling of O is lazy: it happens only when a row's
+// maximum grows by more than 2^8, otherwise the stale maximum is kept (exact, since O and
+// the running sum always share one reference maximum).
+//
+// Barrier phases run across items: every role counts the completions it has consumed
+// (per query tile) and waits on the parity of that count.  No barrier can run two phases
+// ahead of a waiter, because each producer of a phase first waits on a consequence of
+// the previous one.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -42,17 +56,22 @@ namespace {
 constexpr int kD = 128;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kStages = 2;
+constexpr int kSlots = 3;                     // K/V ring depth
 constexpr int kBoxBytes = 128 * 128;          // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr int kTileBytes = 2 * kBoxBytes;     // 128 rows x 128 bf16
-constexpr int kSmemQ = 0;                     // two query tiles
-constexpr int kSmemK = 2 * kTileBytes;
-constexpr int kSmemV = kSmemK + kStages * kTileBytes;
-constexpr int kSmemBar = kSmemV + kStages * kTileBytes;
+constexpr int kSmemQ = 0;                     // 2 buffers x 2 query tiles
+constexpr int kSmemRing = 4 * kTileBytes;
+constexpr int kSmemBar = kSmemRing + kSlots * kTileBytes;
 constexpr int kSmemBytes = kSmemBar + 256 + 1024;  // + barriers + alignment slack
 constexpr int kThreads = 384;
+constexpr int kRotThreads = 64;               // warps 2-3
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
+// Items with at least this many key tiles on average go to the one-CTA-per-item kernel:
+// their per-item fixed work is small next to the item, and the hardware balances uneven
+// causal item lengths better than the static persistent schedule (GB300 measurements:
+// persistent 0.56 vs 0.51 of peak at ~17 tiles per item, 0.68 vs 0.74 at ~128).
+constexpr int kStreamMinTiles = 48;
 // Column pairs (bit i: pair i of each 32-column chunk) whose exponentials run on the FMA
 // pipe (ex2_fma2) instead of the special-function unit.  Off by default: the softmax is
 // bound by instruction issue and latency, not by the special-function unit, so the
@@ -63,14 +82,13 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units
 constexpr uint32_t kPolyPairs = GQA_PREFILL_POLY_PAIRS;
 
 struct Bars {
-    uint64_t q_full;
-    uint64_t q_ready[2];
-    uint64_t k_full[kStages];
-    uint64_t v_full[kStages];
-    uint64_t kv_empty[kStages];
-    uint64_t s_full[2];
-    uint64_t p_full[2];
-    uint64_t o_done[2];
+    uint64_t q_full[2], q_ready[2];               // per Q buffer
+    uint64_t epi_done[2];                         // the buffer's O staging has been stored
+    uint64_t staged[2];                           // per query tile: O rows written to smem
+    uint64_t full[kSlots], empty[kSlots];         // K/V ring
+    uint64_t s_full[2], p_full[2], o_done[2];     // per query tile
+    uint64_t o_final[2];                          // an item's last PV product of the tile
+    uint64_t o_free[2];                           // the epilogue has read O out of TMEM
     uint64_t mma_done;
     uint32_t tmem_base;
 };
@@ -82,9 +100,40 @@ struct Params {
     const float2 *table;
     int *status;
     int T, S, Hq, Hkv, G, window;
-    int n_mblocks, n_pairs;
+    int n_mblocks, n_pairs, n_items;
     float scale_log2;
 };
+
+struct Item {
+    int mb, g, b, h0, kt_first, n_tiles;
+    bool two;
+};
+
+// Item index -> its coordinates; query blocks with the most keys first.
+__device__ __forceinline__ Item make_item(const Params &p, int idx) {
+    Item it;
+    const int pair = idx % p.n_pairs;
+    idx /= p.n_pairs;
+    it.mb = p.n_mblocks - 1 - (idx % p.n_mblocks);
+    idx /= p.n_mblocks;
+    it.g = idx % p.Hkv;
+    it.b = idx / p.Hkv;
+    it.h0 = it.g * p.G + 2 * pair;
+    it.two = (2 * pair + 1) < p.G;
+    const int q_lo = p.S - p.T + it.mb * kBM;                 // position of row 0
+    const int q_hi = min(q_lo + kBM - 1, p.S - 1);            // position of the last row
+    it.kt_first = p.window > 0 ? max(0, q_lo - p.window + 1) / kBN : 0;
+    it.n_tiles = q_hi / kBN - it.kt_first + 1;
+    return it;
+}
+
+// Index of this CTA's k-th item, or -1 past the end.  Round r covers items
+// [r G, (r + 1) G) with G = gridDim.x; odd rounds are walked backwards.
+__device__ __forceinline__ int item_index(const Params &p, int k) {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    const long idx = static_cast<long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+    return idx < p.n_items ? static_cast<int>(idx) : -1;
+}
 
 // A bounded wait whose outcome every lane of the warp agrees on, so the warp-collective
 // tcgen05.ld/st that follow are never reached by only part of a warp.
@@ -92,46 +141,37 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// Roles for the diagnostic code of an expired wait.
+enum Role { kRoleProducer = 0, kRoleMma = 1, kRoleSoftmax = 2, kRoleRope = 3 };
+
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+    prefill_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const Params p) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     Bars *bars = reinterpret_cast<Bars *>(smem + kSmemBar);
-    uint8_t *sQ[2] = {smem + kSmemQ, smem + kSmemQ + kTileBytes};
+    auto sQ = [&](int buf, int i) { return smem + kSmemQ + (2 * buf + i) * kTileBytes; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- work item ----
-    int idx = blockIdx.x;
-    const int pair = idx % p.n_pairs;
-    idx /= p.n_pairs;
-    const int mb = p.n_mblocks - 1 - (idx % p.n_mblocks);  // longest rows first
-    idx /= p.n_mblocks;
-    const int g = idx % p.Hkv;
-    const int b = idx / p.Hkv;
-    const int h0 = g * p.G + 2 * pair;
-    const bool two = (2 * pair + 1) < p.G;
-    const int q_lo = p.S - p.T + mb * kBM;                   // position of row 0
-    const int q_hi = min(q_lo + kBM - 1, p.S - 1);           // position of the last row
-    const int kt_first = p.window > 0 ? max(0, q_lo - p.window + 1) / kBN : 0;
-    const int kt_last = q_hi / kBN;
-    const int n_tiles = kt_last - kt_first + 1;
-
     if (threadIdx.x == 0) {
-        mbar_init(&bars->q_full, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->q_ready[i], 128);
+            mbar_init(&bars->q_full[i], 1);
+            mbar_init(&bars->q_ready[i], kRotThreads);
+            mbar_init(&bars->epi_done[i], 2);
+            mbar_init(&bars->staged[i], 128);
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->p_full[i], 128);
             mbar_init(&bars->o_done[i], 1);
+            mbar_init(&bars->o_final[i], 1);
+            mbar_init(&bars->o_free[i], 128);
         }
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->k_full[s], 1);
-            mbar_init(&bars->v_full[s], 1);
-            mbar_init(&bars->kv_empty[s], 1);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
         }
         mbar_init(&bars->mma_done, 1);
         fence_mbar_init();
@@ -151,38 +191,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            const int zq = b * p.Hq + h0;
-            mbar_arrive_expect_tx(&bars->q_full, (two ? 2 : 1) * kTileBytes);
-            for (int i = 0; i < (two ? 2 : 1); ++i) {
-                tma_load_3d(sQ[i], &tmQ, &bars->q_full, 0, mb * kBM, zq + i);
-                tma_load_3d(sQ[i] + kBoxBytes, &tmQ, &bars->q_full, 64, mb * kBM, zq + i);
-            }
-            const int zk = b * p.Hkv + g;
+            tma_prefetch_desc(&tmO);
             bool ok = true;
-            int issued = 0;
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int s = j % kStages;
-                if (j >= kStages && !mbar_wait(&bars->kv_empty[s], ((j / kStages) - 1) & 1)) {
-                    set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
-                    ok = false;
-                    break;
+            int u = 0;          // ring loads issued
+            int q_issued = 0;   // items whose Q tiles have been issued
+            auto load_q = [&](int k) {
+                const Item it = make_item(p, item_index(p, k));
+                const int buf = k & 1;
+                // buffer reuse: item k - 2 is finished and its O, staged in this buffer,
+                // has been read out by the TMA stores
+                if (k >= 2 && !(ok = mbar_wait(&bars->epi_done[buf], ((k - 2) >> 1) & 1))) {
+                    set_timeout(p.status, kDiagPrefill, kRoleProducer, 0, k);
+                    return;
                 }
-                const int n0 = (kt_first + j) * kBN;
-                uint8_t *sK = smem + kSmemK + s * kTileBytes;
-                uint8_t *sV = smem + kSmemV + s * kTileBytes;
-                mbar_arrive_expect_tx(&bars->k_full[s], kTileBytes);
-                tma_load_3d(sK, &tmK, &bars->k_full[s], 0, n0, zk);
-                tma_load_3d(sK + kBoxBytes, &tmK, &bars->k_full[s], 64, n0, zk);
-                mbar_arrive_expect_tx(&bars->v_full[s], kTileBytes);
-                tma_load_3d(sV, &tmV, &bars->v_full[s], 0, n0, zk);
-                tma_load_3d(sV + kBoxBytes, &tmV, &bars->v_full[s], 64, n0, zk);
-                issued = j + 1;
+                const int zq = it.b * p.Hq + it.h0;
+                mbar_arrive_expect_tx(&bars->q_full[buf], (it.two ? 2 : 1) * kTileBytes);
+                for (int i = 0; i < (it.two ? 2 : 1); ++i) {
+                    tma_load_3d(sQ(buf, i), &tmQ, &bars->q_full[buf], 0, it.mb * kBM, zq + i);
+                    tma_load_3d(sQ(buf, i) + kBoxBytes, &tmQ, &bars->q_full[buf], 64,
+                                it.mb * kBM, zq + i);
+                }
+                q_issued = k + 1;
+            };
+            auto put = [&](const CUtensorMap *map, int n0, int zk) {
+                const int st = u % kSlots;
+                if (u >= kSlots && !(ok = mbar_wait(&bars->empty[st], ((u / kSlots) - 1) & 1))) {
+                    set_timeout(p.status, kDiagPrefill, kRoleProducer, 1, u);
+                    return;
+                }
+                uint8_t *dst = smem + kSmemRing + st * kTileBytes;
+                mbar_arrive_expect_tx(&bars->full[st], kTileBytes);
+                tma_load_3d(dst, map, &bars->full[st], 0, n0, zk);
+                tma_load_3d(dst + kBoxBytes, map, &bars->full[st], 64, n0, zk);
+                ++u;
+            };
+            if (item_index(p, 0) >= 0) load_q(0);
+            for (int k = 0; ok && item_index(p, k) >= 0; ++k) {
+                const Item it = make_item(p, item_index(p, k));
+                const bool has_next = item_index(p, k + 1) >= 0;
+                const int zk = it.b * p.Hkv + it.g;
+                // K(0), V(0), K(1), V(1), ...; the next item's Q after the fourth load, by
+                // which time the MMA thread has moved on to this item
+                const int n_loads = 2 * it.n_tiles;
+                const int q_at = min(3, n_loads - 1);
+                for (int l = 0; l < n_loads && ok; ++l) {
+                    const int n0 = (it.kt_first + (l >> 1)) * kBN;
+                    put((l & 1) ? &tmV : &tmK, n0, zk);
+                    if (l == q_at && has_next && ok) load_q(k + 1);
+                }
             }
-            // never leave the CTA with copies in flight
-            mbar_wait(&bars->q_full, 0);
-            for (int j = max(0, issued - kStages); j < issued; ++j) {
-                mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1);
-                mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1);
+            if (!ok) {
+                // never leave the CTA with copies in flight
+                for (int w = max(0, u - kSlots); w < u; ++w)
+                    mbar_wait(&bars->full[w % kSlots], (w / kSlots) & 1);
+                for (int k = max(0, q_issued - 2); k < q_issued; ++k)
+                    mbar_wait(&bars->q_full[k & 1], (k >> 1) & 1);
             }
         }
         __syncwarp();
@@ -191,22 +254,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
             const uint32_t idesc_o = idesc_bf16_f32(kBM, kD, 0, 1);
-            const uint32_t qaddr[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
-            const uint32_t kaddr0 = smem_u32(smem + kSmemK), vaddr0 = smem_u32(smem + kSmemV);
-            const int ntile = two ? 2 : 1;
+            const uint32_t ring0 = smem_u32(smem + kSmemRing);
             bool ok = true;
-            auto issue_s = [&](int i, int s) {
-                const uint32_t ka = kaddr0 + s * kTileBytes;
+            int u = 0;                 // ring slots consumed
+            int cpv[2] = {0, 0};       // PV products issued, per query tile (all items)
+            int nepi[2] = {0, 0};      // items finished, per query tile
+            auto take = [&](int &st) {
+                st = u % kSlots;
+                if (!(ok = mbar_wait(&bars->full[st], (u / kSlots) & 1))) {
+                    set_timeout(p.status, kDiagPrefill, kRoleMma, 1, u);
+                    return;
+                }
+                ++u;
+                tc_fence_after();
+            };
+            auto issue_s = [&](uint32_t qaddr, int i, int st) {
+                const uint32_t ka = ring0 + st * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                    umma_ss(tmem + i * 128, sdesc_sw128(qaddr[i] + off, 16, 1024),
+                    umma_ss(tmem + i * 128, sdesc_sw128(qaddr + off, 16, 1024),
                             sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&bars->s_full[i]);
             };
-            auto issue_pv = [&](int i, int s, bool acc) {
-                const uint32_t va = vaddr0 + s * kTileBytes;
+            auto issue_pv = [&](int i, int st, bool acc) {
+                const uint32_t va = ring0 + st * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     umma_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
@@ -214,35 +287,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (acc || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(&bars->o_done[i]);
+                ++cpv[i];
             };
-            for (int i = 0; i < ntile && ok; ++i) ok = mbar_wait(&bars->q_ready[i], 0);
-            tc_fence_after();
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int s = j % kStages;
-                const uint32_t par = (j / kStages) & 1;
-                if (j == 0) {
-                    if (!(ok = mbar_wait(&bars->k_full[s], par))) break;
-                    tc_fence_after();
-                    for (int i = 0; i < ntile; ++i) issue_s(i, s);
+            // waits until PV product number cpv[i] - 1 of tile i has completed
+            auto wait_last_pv = [&](int i, int where) {
+                if (cpv[i] > 0 && !(ok = mbar_wait(&bars->o_done[i], (cpv[i] - 1) & 1)))
+                    set_timeout(p.status, kDiagPrefill, kRoleMma, where, cpv[i]);
+                tc_fence_after();
+            };
+            for (int k = 0; ok && item_index(p, k) >= 0; ++k) {
+                const Item it = make_item(p, item_index(p, k));
+                const int buf = k & 1, ntile = it.two ? 2 : 1, n = it.n_tiles;
+                const uint32_t qaddr[2] = {smem_u32(sQ(buf, 0)), smem_u32(sQ(buf, 1))};
+                if (!(ok = mbar_wait(&bars->q_ready[buf], (k >> 1) & 1))) {
+                    set_timeout(p.status, kDiagPrefill, kRoleMma, 0, k);
+                    break;
                 }
-                if (!(ok = mbar_wait(&bars->v_full[s], par))) break;
-                const int s1 = (j + 1) % kStages;
-                const uint32_t par1 = ((j + 1) / kStages) & 1;
+                tc_fence_after();
+                int kst = 0, vst = 0;
+                take(kst);
                 for (int i = 0; i < ntile && ok; ++i) {
-                    if (!(ok = mbar_wait(&bars->p_full[i], j & 1))) break;
-                    tc_fence_after();
-                    issue_pv(i, s, j > 0);
-                    if (i == ntile - 1) umma_commit(&bars->kv_empty[s]);
-                    if (j + 1 < n_tiles) {
-                        if (i == 0 && !(ok = mbar_wait(&bars->k_full[s1], par1))) break;
-                        // S_i(j+1) overwrites the TMEM columns P_i(j) sits in; the tensor
-                        // pipe does not order that write after PV_i(j)'s read, so wait for
-                        // PV_i(j) to complete first
-                        if (!(ok = mbar_wait(&bars->o_done[i], j & 1))) break;
-                        tc_fence_after();
-                        issue_s(i, s1);
-                    }
+                    // S_i(0) overwrites the columns the previous item's last P_i sits in
+                    wait_last_pv(i, 2);
+                    if (ok) issue_s(qaddr[i], i, kst);
                 }
+                if (!ok) break;
+                umma_commit(&bars->empty[kst]);
+                for (int j = 0; j < n && ok; ++j) {
+                    take(vst);
+                    for (int i = 0; i < ntile && ok; ++i) {
+                        if (!(ok = mbar_wait(&bars->p_full[i], cpv[i] & 1))) {
+                            set_timeout(p.status, kDiagPrefill, kRoleMma, 3, cpv[i]);
+                            break;
+                        }
+                        // the first PV of an item overwrites O_i: the previous item's
+                        // epilogue must have read it out
+                        if (j == 0 && nepi[i] > 0 &&
+                            !(ok = mbar_wait(&bars->o_free[i], (nepi[i] - 1) & 1))) {
+                            set_timeout(p.status, kDiagPrefill, kRoleMma, 4, nepi[i]);
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(i, vst, j > 0);
+                        if (j == n - 1) umma_commit(&bars->o_final[i]);
+                        if (j + 1 < n) {
+                            if (i == 0) take(kst);
+                            if (!ok) break;
+                            // S_i(j+1) overwrites the columns P_i(j) sits in
+                            wait_last_pv(i, 5);
+                            if (ok) issue_s(qaddr[i], i, kst);
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(&bars->empty[vst]);
+                    if (j + 1 < n) umma_commit(&bars->empty[kst]);
+                }
+                if (!ok) break;
+                for (int i = 0; i < ntile; ++i) ++nepi[i];
             }
             if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
             // every tcgen05 operation issued above completes before TMEM is released
@@ -250,71 +351,90 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&bars->mma_done, 0);
         }
         __syncwarp();
-    } else if (warp >= 4) {
-        // ================= softmax / epilogue =================
-        const int wg = (warp - 4) >> 2;      // query tile
-        const int r = (warp & 3) * 32 + lane;  // row in tile == TMEM lane
-        const bool tile_on = (wg == 0) || two;
-        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_off + wg * 128;
-        const uint32_t tO = tmem + lane_off + 256 + wg * 128;
-        const int t = mb * kBM + r;
-        const bool valid = t < p.T;
-        const int qpos = p.S - p.T + t;
-        const int h = h0 + wg;
-        bool ok = true;
-
-        if (tile_on) {
-            // ---- RoPE on the Q row in shared memory (128-byte swizzle: 16-byte chunk c of
-            // row r sits at chunk c ^ (r & 7); pair (j, j + 64) = same offset in box 0 / 1)
-            // the row's table entries are fetched while the Q tile is still in flight
-            float4 tq[32];
-            {
-                const float4 *t4 = reinterpret_cast<const float4 *>(
-                    p.table + (size_t)(valid ? qpos : 0) * (kD / 2));
-#pragma unroll
-                for (int i = 0; i < 32; ++i) tq[i] = __ldg(t4 + i);
+    } else if (warp < 4) {
+        // ================= RoPE on Q tiles (warps 2-3) =================
+        // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7); the pair
+        // (j, j + 64) is the same offset in box 0 and box 1
+        const int rt = threadIdx.x - 64;   // 0..63
+        for (int k = 0; item_index(p, k) >= 0; ++k) {
+            const Item it = make_item(p, item_index(p, k));
+            const int buf = k & 1;
+            if (!warp_wait(&bars->q_full[buf], (k >> 1) & 1)) {
+                set_timeout(p.status, kDiagPrefill, kRoleRope, 0, k);
+                break;
             }
-            ok = warp_wait(&bars->q_full, 0);
-            if (ok && valid) {
-                uint8_t *row0 = sQ[wg] + r * 128;
-                uint8_t *row1 = row0 + kBoxBytes;
+            for (int i = 0; i < (it.two ? 2 : 1); ++i) {
+                for (int rr = 0; rr < kBM / kRotThreads; ++rr) {
+                    const int r = rt + kRotThreads * rr;
+                    const int t = it.mb * kBM + r;
+                    if (t >= p.T) continue;
+                    const float4 *t4 = reinterpret_cast<const float4 *>(
+                        p.table + (size_t)(p.S - p.T + t) * (kD / 2));
+                    uint8_t *row0 = sQ(buf, i) + r * 128;
+                    uint8_t *row1 = row0 + kBoxBytes;
+#pragma unroll 2
+                    for (int c = 0; c < 8; ++c) {
+                        const int pc = (c ^ (r & 7)) * 16;
+                        const uint4 a = *reinterpret_cast<uint4 *>(row0 + pc);
+                        const uint4 bq = *reinterpret_cast<uint4 *>(row1 + pc);
+                        float cs[16];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int pc = (c ^ (r & 7)) * 16;
-                    uint4 a = *reinterpret_cast<uint4 *>(row0 + pc);
-                    uint4 bq = *reinterpret_cast<uint4 *>(row1 + pc);
-                    float cs[16];
+                        for (int qq = 0; qq < 4; ++qq) {
+                            const float4 tv = __ldg(t4 + 4 * c + qq);
+                            cs[4 * qq] = tv.x;
+                            cs[4 * qq + 1] = tv.y;
+                            cs[4 * qq + 2] = tv.z;
+                            cs[4 * qq + 3] = tv.w;
+                        }
+                        uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bq.x, bq.y, bq.z, bq.w};
 #pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) {
-                        const float4 tv = tq[4 * c + qq];
-                        cs[4 * qq] = tv.x;
-                        cs[4 * qq + 1] = tv.y;
-                        cs[4 * qq + 2] = tv.z;
-                        cs[4 * qq + 3] = tv.w;
+                        for (int qq = 0; qq < 4; ++qq) {
+                            const float a0 = bf16lo(aw[qq]), a1 = bf16hi(aw[qq]);
+                            const float b0 = bf16lo(bw[qq]), b1 = bf16hi(bw[qq]);
+                            const float c0 = cs[4 * qq], s0 = cs[4 * qq + 1];
+                            const float c1 = cs[4 * qq + 2], s1 = cs[4 * qq + 3];
+                            aw[qq] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
+                            bw[qq] = pack_bf16x2(fmaf(a0, s0, b0 * c0), fmaf(a1, s1, b1 * c1));
+                        }
+                        *reinterpret_cast<uint4 *>(row0 + pc) =
+                            make_uint4(aw[0], aw[1], aw[2], aw[3]);
+                        *reinterpret_cast<uint4 *>(row1 + pc) =
+                            make_uint4(bw[0], bw[1], bw[2], bw[3]);
                     }
-                    uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) {
-                        const float a0 = bf16lo(aw[qq]), a1 = bf16hi(aw[qq]);
-                        const float b0 = bf16lo(bw[qq]), b1 = bf16hi(bw[qq]);
-                        const float c0 = cs[4 * qq], s0 = cs[4 * qq + 1];
-                        const float c1 = cs[4 * qq + 2], s1 = cs[4 * qq + 3];
-                        aw[qq] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
-                        bw[qq] = pack_bf16x2(fmaf(a0, s0, b0 * c0), fmaf(a1, s1, b1 * c1));
-                    }
-                    *reinterpret_cast<uint4 *>(row0 + pc) = make_uint4(aw[0], aw[1], aw[2], aw[3]);
-                    *reinterpret_cast<uint4 *>(row1 + pc) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(&bars->q_ready[wg]);
+            mbar_arrive(&bars->q_ready[buf]);
         }
-
-        float m = -CUDART_INF_F, l = 0.f;
-        if (tile_on && ok) {
+    } else {
+        // ================= softmax / epilogue =================
+        const int wg = (warp - 4) >> 2;      // query tile
+        const int r = (warp & 3) * 32 + lane;  // row in tile == TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_off + wg * 128;
+        const uint32_t tO = tmem + lane_off + 256 + wg * 128;
+        int cs = 0;    // score tiles consumed (all items)
+        int pvb = 0;   // PV products of the previous items
+        int ne = 0;    // items finished
+        bool ok = true;
+        for (int k = 0; ok && item_index(p, k) >= 0; ++k) {
+            int n_tiles, kt_first, qpos;
+            {
+                const Item it = make_item(p, item_index(p, k));
+                if (wg == 1 && !it.two) continue;
+                n_tiles = it.n_tiles;
+                kt_first = it.kt_first;
+                qpos = p.S - p.T + it.mb * kBM + r;
+            }
+            const bool valid = qpos < p.S;   // the row exists (t < T)
+            float m = -CUDART_INF_F, l = 0.f;
             for (int j = 0; j < n_tiles; ++j) {
-                if (!warp_wait(&bars->s_full[wg], j & 1)) { ok = false; break; }
+                if (!warp_wait(&bars->s_full[wg], cs & 1)) {
+                    set_timeout(p.status, kDiagPrefill, kRoleSoftmax, 0, cs);
+                    ok = false;
+                    break;
+                }
+                ++cs;
                 tc_fence_after();
                 const int n0 = (kt_first + j) * kBN;
                 const bool full = valid && (n0 + kBN - 1 <= qpos) &&
@@ -343,12 +463,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // row maximum of the raw scores: 3-input max, 8 independent chains of 16
                 float mx8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    mx8[k] = fmax3(x[k], x[k + 8], x[k + 16]);
+                for (int kk = 0; kk < 8; ++kk) {
+                    mx8[kk] = fmax3(x[kk], x[kk + 8], x[kk + 16]);
 #pragma unroll
-                    for (int t = 3; t < 15; t += 2)
-                        mx8[k] = fmax3(mx8[k], x[k + 8 * t], x[k + 8 * t + 8]);
-                    mx8[k] = fmaxf(mx8[k], x[k + 120]);
+                    for (int tt = 3; tt < 15; tt += 2)
+                        mx8[kk] = fmax3(mx8[kk], x[kk + 8 * tt], x[kk + 8 * tt + 8]);
+                    mx8[kk] = fmaxf(mx8[kk], x[kk + 120]);
                 }
                 const float mraw = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                                          fmaxf(mx8[6], mx8[7]));
@@ -390,9 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) +
                      ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
                 if (__any_sync(0xffffffffu, need_o)) {
-                    // O still holds the product of tiles < j: wait for the last one, then
-                    // rescale it in TMEM before this tile's PV is issued.
-                    if (!warp_wait(&bars->o_done[wg], (j - 1) & 1)) ok = false;
+                    // O holds the product of tiles < j (already complete: S_i(j) was
+                    // issued after PV_i(j-1) finished); rescale it in TMEM before this
+                    // tile's PV is issued
+                    if (!warp_wait(&bars->o_done[wg], (pvb + j - 1) & 1)) {
+                        set_timeout(p.status, kDiagPrefill, kRoleSoftmax, 1, pvb + j);
+                        ok = false;
+                    }
                     tc_fence_after();
                     const float fo = need_o ? f : 1.0f;
 #pragma unroll 1
@@ -411,37 +535,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bars->p_full[wg]);
                 if (!ok) break;
             }
-            if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
-            // ---- epilogue: O / l -> bf16, lse
-            if (ok && warp_wait(&bars->o_done[wg], (n_tiles - 1) & 1)) {
-                tc_fence_after();
-                const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-                __nv_bfloat16 *orow = p.o + (((size_t)b * p.Hq + h) * p.T + t) * kD;
+            if (!ok) break;
+            pvb += n_tiles;
+            // ---- epilogue: O out of TMEM first (frees it for the next item); O / l as
+            // bf16 into this item's Q buffer (every score product has completed, so the
+            // buffer is free), in the 128-byte-swizzled layout of a Q tile; one TMA store
+            // per 64-column box writes it out (rows past T are clipped by the tensor map)
+            if (!warp_wait(&bars->o_final[wg], ne & 1)) {
+                set_timeout(p.status, kDiagPrefill, kRoleSoftmax, 2, ne);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            {
+                float x[128];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t rr[32];
                     tmem_ld32(tO + 32 * c, rr);
-                    tmem_wait_ld();
-                    if (valid) {
-                        uint32_t pkd[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pkd[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
-                                                 __uint_as_float(rr[2 * i + 1]) * inv_l);
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2],
-                                                pkd[4 * i + 3]);
-                    }
+                    for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(rr[i]);
                 }
-                if (valid && p.lse)
-                    p.lse[((size_t)b * p.Hq + h) * p.T + t] =
-                        (m + __log2f(l)) * 0.69314718055994531f;
-            } else if (ok) {
-                set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&bars->o_free[wg]);
+                const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+                uint8_t *stage = sQ(k & 1, wg) + r * 128;
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    *reinterpret_cast<uint4 *>(stage + (c >> 3) * kBoxBytes +
+                                               (((c & 7) ^ (r & 7)) << 4)) =
+                        make_uint4(pack_bf16x2(x[8 * c] * inv_l, x[8 * c + 1] * inv_l),
+                                   pack_bf16x2(x[8 * c + 2] * inv_l, x[8 * c + 3] * inv_l),
+                                   pack_bf16x2(x[8 * c + 4] * inv_l, x[8 * c + 5] * inv_l),
+                                   pack_bf16x2(x[8 * c + 6] * inv_l, x[8 * c + 7] * inv_l));
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->staged[wg]);
+            const Item it = make_item(p, item_index(p, k));
+            if (r == 0) {
+                if (!mbar_wait(&bars->staged[wg], ne & 1)) {
+                    set_timeout(p.status, kDiagPrefill, kRoleSoftmax, 3, ne);
+                    ok = false;
+                } else {
+                    const int zo = it.b * p.Hq + it.h0 + wg;
+                    tma_store_3d(&tmO, sQ(k & 1, wg), 0, it.mb * kBM, zo);
+                    tma_store_3d(&tmO, sQ(k & 1, wg) + kBoxBytes, 64, it.mb * kBM, zo);
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                    // the buffer's second arrival comes from tile 1, or from here if the
+                    // item has no tile 1
+                    mbar_arrive_cnt(&bars->epi_done[k & 1], it.two ? 1 : 2);
+                }
+            }
+            ++ne;
+            if (valid && p.lse) {
+                const int t = it.mb * kBM + r;
+                p.lse[((size_t)it.b * p.Hq + it.h0 + wg) * p.T + t] =
+                    (m + __log2f(l)) * 0.69314718055994531f;
             }
         }
+        // the O stores complete before the CTA exits
+        if (r == 0) bulk_wait_all();
+        if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
     }
 
     tc_fence_before();
@@ -493,14 +649,31 @@ int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, flo
                    const float *table, int table_len, int *status, cudaStream_t s) {
     (void)table_len;
     if (d != kD) return GQA_ERR_UNSUPPORTED;
-    CUtensorMap mq, mk, mv;
+    {
+        // long items (a causal sweep over a long sequence): one CTA per item
+        const int n_mb = (T + kBM - 1) / kBM;
+        long tiles = 0;
+        for (int mb = 0; mb < n_mb; ++mb) {
+            const int q_lo = S - T + mb * kBM, q_hi = (q_lo + kBM - 1 < S - 1) ? q_lo + kBM - 1 : S - 1;
+            const int kt0 = window > 0 ? (q_lo - window + 1 > 0 ? q_lo - window + 1 : 0) / kBN : 0;
+            tiles += q_hi / kBN - kt0 + 1;
+        }
+        if (tiles >= (long)kStreamMinTiles * n_mb)
+            return launch_prefill_stream(q, k_rot, v, o, lse, B, T, S, Hq, Hkv, d, window, scale,
+                                         table, status, s);
+    }
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, q, d, T, B * Hq) || !make_map(&mk, k_rot, d, S, B * Hkv) ||
-        !make_map(&mv, v, d, S, B * Hkv))
+        !make_map(&mv, v, d, S, B * Hkv) || !make_map(&mo, o, d, T, B * Hq))
         return GQA_ERR_CUDA;
     static bool attr_done = false;
+    static int sm_count = 0;
     if (!attr_done) {
-        if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess)
+        int dev = 0;
+        if (cudaFuncSetAttribute(prefill_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess ||
+            cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return GQA_ERR_CUDA;   // the error stays readable with cudaGetLastError
         attr_done = true;
     }
@@ -518,8 +691,11 @@ int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, flo
     p.n_mblocks = (T + kBM - 1) / kBM;
     p.n_pairs = (p.G + 1) / 2;
     p.scale_log2 = scale * 1.4426950408889634f;
-    const long nblocks = (long)B * Hkv * p.n_pairs * p.n_mblocks;
-    prefill_kernel<<<static_cast<unsigned>(nblocks), kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+    const long n_items = (long)B * Hkv * p.n_pairs * p.n_mblocks;
+    if (n_items > 0x7fffffffL) return GQA_ERR_UNSUPPORTED;
+    p.n_items = static_cast<int>(n_items);
+    const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
+    prefill_persistent_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, p);
     const cudaError_t e = cudaPeekAtLastError();
     return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }

@@ -166,3 +166,21 @@ def test_full_size_repeat_bitwise(name, index):
     for _ in range(6):
         o, lse = gu.run_prefill(q, k, v, layer.window, layer.scale, table, layer.S)
         assert torch.equal(o, first) and torch.equal(lse, first_lse)
+
+
+def test_persistent_odd_group_many_items_sampled():
+    """Windowed layer with more items than SMs (each persistent CTA walks several) and an
+    odd group size, so single-tile items alternate with two-tile ones."""
+    layer = _layer(1, 8192, 8192, 12, 4, 256, seed=81)
+    from global_causal_gqa_gb300 import accounting as acc
+    assert acc.prefill_d128_kernel(layer.T, layer.S, layer.window) == "prefill_persistent_kernel"
+    _sampled_case(layer, 2048, 6)
+
+
+def test_stream_kernel_medium_causal_sampled():
+    """Causal sweep long enough (mean >= 48 key tiles per query block) for the
+    one-CTA-per-item kernel, with a ragged last block and queries after a longer history."""
+    layer = _layer(1, 12200, 12300, 4, 2, 0, YARN, seed=82)
+    from global_causal_gqa_gb300 import accounting as acc
+    assert acc.prefill_d128_kernel(layer.T, layer.S, layer.window) == "prefill_kernel"
+    _sampled_case(layer, 2048, 7)
