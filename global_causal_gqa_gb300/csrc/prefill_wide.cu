@@ -58,6 +58,7 @@ struct WBars {
     // last tile PV(n-2) may still run and o_done can be two phases behind -- its parity
     // would then already read as "done" for PV(n-1)
     uint64_t o_final;
+    uint64_t staged;          // O rows written to the shared-memory staging area
     uint32_t tmem_base;
 };
 static_assert(sizeof(WBars) <= 256, "barrier block");
@@ -80,7 +81,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_wide_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, const WParams p) {
+                        const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmO, const WParams p) {
     constexpr int BN = Wide<D>::BN, DV = Wide<D>::DV, NS = Wide<D>::NS;
     constexpr int NKC = D / 128;                  // 128-dim K chunks per key tile
     constexpr int NVH = DV / 128;                 // 128-dim V halves per key tile
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->p_full[1], 128);
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->o_final, 1);
+        mbar_init(&bars->staged, 128);
         mbar_init(&bars->mma_done, 1);
         fence_mbar_init();
     }
@@ -279,19 +282,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && valid) {
             // RoPE on the Q row: pair (j, j + D/2) = same swizzled offset in boxes k, k + D/128
             const float2 *tab = p.table + (size_t)qpos * (D / 2);
-            for (int kb = 0; kb < D / 128; ++kb) {
+            for (int kc = 0; kc < 2 * (D / 128); ++kc) {
+                const int kb = kc >> 1;
                 uint8_t *row0 = sQ + kb * QBOX + r * 128;
                 uint8_t *row1 = row0 + (D / 128) * QBOX;
-#pragma unroll 2
-                for (int c = 0; c < 8; ++c) {
+                // the table entries of four chunks in flight at once
+                float4 tv4[16];
+                const float4 *t4 = reinterpret_cast<const float4 *>(tab + 64 * kb + 32 * (kc & 1));
+#pragma unroll
+                for (int i = 0; i < 16; ++i) tv4[i] = __ldg(t4 + i);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c = 4 * (kc & 1) + cc;
                     const int pc = (c ^ (r & 7)) * 16;
                     uint4 a = *reinterpret_cast<uint4 *>(row0 + pc);
                     uint4 bq = *reinterpret_cast<uint4 *>(row1 + pc);
-                    const float4 *t4 = reinterpret_cast<const float4 *>(tab + 64 * kb + 8 * c);
                     float cs[16];
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) {
-                        const float4 tv = __ldg(t4 + qq);
+                        const float4 tv = tv4[4 * cc + qq];
                         cs[4 * qq] = tv.x;
                         cs[4 * qq + 1] = tv.y;
                         cs[4 * qq + 2] = tv.z;
@@ -406,26 +415,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
         if (ok && warp_wait_w(&bars->o_final, 0)) {
+            // O / l as bf16 into the Q buffer (every score product has completed), in the
+            // 128-byte-swizzled layout of 64-column boxes; TMA stores write it out (rows
+            // past T are clipped by the tensor map)
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-            __nv_bfloat16 *orow =
-                p.o + (((size_t)b * p.Hq + h) * p.T + t) * D + (size_t)slice * DV;
 #pragma unroll 1
             for (int c = 0; c < DV / 32; ++c) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + lane_off + TO + 32 * c, rr);
                 tmem_wait_ld();
-                if (valid) {
-                    uint32_t pkd[16];
+                uint8_t *box = sQ + (c >> 1) * QBOX + r * 128;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pkd[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l,
-                                             __uint_as_float(rr[2 * i + 1]) * inv_l);
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2],
-                                            pkd[4 * i + 3]);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int cc = 4 * (c & 1) + q4;   // 16-byte chunk within the box row
+                    *reinterpret_cast<uint4 *>(box + ((cc ^ (r & 7)) << 4)) = make_uint4(
+                        pack_bf16x2(__uint_as_float(rr[8 * q4]) * inv_l,
+                                    __uint_as_float(rr[8 * q4 + 1]) * inv_l),
+                        pack_bf16x2(__uint_as_float(rr[8 * q4 + 2]) * inv_l,
+                                    __uint_as_float(rr[8 * q4 + 3]) * inv_l),
+                        pack_bf16x2(__uint_as_float(rr[8 * q4 + 4]) * inv_l,
+                                    __uint_as_float(rr[8 * q4 + 5]) * inv_l),
+                        pack_bf16x2(__uint_as_float(rr[8 * q4 + 6]) * inv_l,
+                                    __uint_as_float(rr[8 * q4 + 7]) * inv_l));
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->staged);
+            if (r == 0) {
+                if (!mbar_wait(&bars->staged, 0)) {
+                    set_timeout(p.status, kDiagPrefillWide, 3, 10, n_tiles);
+                } else {
+                    for (int bx = 0; bx < DV / 64; ++bx)
+                        tma_store_3d(&tmO, sQ + bx * QBOX, slice * DV + 64 * bx, mb * kBM,
+                                     b * p.Hq + h);
+                    bulk_commit_group();
+                    bulk_wait_all();   // complete before the CTA (and its shared memory) ends
                 }
             }
             if (valid && p.lse && slice == 0)
@@ -485,9 +510,9 @@ int launch_wide(const void *q, const void *k_rot, const void *v, void *o, float 
                 int T, int S, int Hq, int Hkv, int window, float scale, const float *table,
                 int *status, cudaStream_t s) {
     constexpr int BN = Wide<D>::BN, DV = Wide<D>::DV;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map_wide(&mq, q, D, T, B * Hq, kBM) || !make_map_wide(&mk, k_rot, D, S, B * Hkv, BN) ||
-        !make_map_wide(&mv, v, D, S, B * Hkv, BN))
+        !make_map_wide(&mv, v, D, S, B * Hkv, BN) || !make_map_wide(&mo, o, D, T, B * Hq, kBM))
         return GQA_ERR_CUDA;
     constexpr int smem = wide_smem_bytes<D>();
     static bool attr_done = false;
@@ -512,7 +537,7 @@ int launch_wide(const void *q, const void *k_rot, const void *v, void *o, float 
     p.n_slices = D / DV;
     p.scale_log2 = scale * 1.4426950408889634f;
     const long nblocks = (long)B * Hq * p.n_mblocks * p.n_slices;
-    prefill_wide_kernel<D><<<static_cast<unsigned>(nblocks), kThreads, smem, s>>>(mq, mk, mv, p);
+    prefill_wide_kernel<D><<<static_cast<unsigned>(nblocks), kThreads, smem, s>>>(mq, mk, mv, mo, p);
     return cudaPeekAtLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
