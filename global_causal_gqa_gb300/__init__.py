@@ -24,6 +24,7 @@ __all__ = [
     "gqa_rope_inv_freq", "gqa_yarn_amplitude", "gqa_rope_table_bytes", "gqa_rope_table_build",
     "gqa_rope_apply", "gqa_prefill_workspace_bytes", "gqa_attn_prefill", "gqa_kv_append",
     "gqa_decode_workspace_bytes", "gqa_attn_decode", "gqa_attn_decode_static",
+    "gqa_qk_norm_rope", "gqa_qk_norm_append",
     "gqa_get_device_status", "gqa_get_device_diag", "gqa_watchdog_selftest",
     "gqa_status_string", "gqa_last_error_string", "gqa_device_check",
 ]
@@ -79,6 +80,8 @@ def lib() -> ctypes.CDLL:
             "gqa_decode_workspace_bytes": ([I, I, I, I], Z),
             "gqa_attn_decode": ([P, P, I, I, I, I, F, I, P, P, P, Z, P], I),
             "gqa_attn_decode_static": ([P, P, I, I, I, I, F, I, P, P, P], I),
+            "gqa_qk_norm_rope": ([P, P, P, P, P, I, I, I, I, I, I, P, P, F, P, I, P], I),
+            "gqa_qk_norm_append": ([P, I, P, P, P, I, I, I, P, P, F, I, P, P, P], I),
             "gqa_get_device_status": ([P], I),
             "gqa_get_device_diag": ([P, P, I], I),
             "gqa_watchdog_selftest": ([ctypes.c_int64, P], I),
@@ -212,6 +215,26 @@ def gqa_attn_decode_static(q, descs, nseq: int, Hq: int, Hkv: int, d: int, scale
     st = lib().gqa_attn_decode_static(_ptr(q), _ptr(descs), nseq, Hq, Hkv, d, scale, max_len,
                                       _ptr(o), _ptr(lse), _stream(stream))
     return _check("gqa_attn_decode_static", st, check)
+
+
+# ---- Q/K normalisation ------------------------------------------------------------------------
+
+def gqa_qk_norm_rope(q, k, q_out, k_out, k_rot, B: int, Hq: int, Hkv: int, T: int, d: int,
+                     pos0: int, q_gamma, k_gamma, eps: float, table, table_len: int,
+                     stream=None, check: bool = True) -> int:
+    st = lib().gqa_qk_norm_rope(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _ptr(k_rot), B, Hq,
+                                Hkv, T, d, pos0, _ptr(q_gamma), _ptr(k_gamma), eps, _ptr(table),
+                                table_len, _stream(stream))
+    return _check("gqa_qk_norm_rope", st, check)
+
+
+def gqa_qk_norm_append(descs, nseq: int, q, k_new, v_new, Hq: int, Hkv: int, d: int, q_gamma,
+                       k_gamma, eps: float, v_norm: int, q_out, slots_out=None, stream=None,
+                       check: bool = True) -> int:
+    st = lib().gqa_qk_norm_append(_ptr(descs), nseq, _ptr(q), _ptr(k_new), _ptr(v_new), Hq, Hkv,
+                                  d, _ptr(q_gamma), _ptr(k_gamma), eps, v_norm, _ptr(q_out),
+                                  _ptr(slots_out), _stream(stream))
+    return _check("gqa_qk_norm_append", st, check)
 
 
 # ---- status ---------------------------------------------------------------------------------

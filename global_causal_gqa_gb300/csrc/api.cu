@@ -177,6 +177,43 @@ gqa_status gqa_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new, const 
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
+gqa_status gqa_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out, void *k_rot,
+                            int B, int Hq, int Hkv, int T, int d, int pos0,
+                            const float *q_gamma, const float *k_gamma, float eps,
+                            const float *table, int table_len, gqa_stream_t stream) {
+    if (!q || !k || !q_out || !q_gamma || !k_gamma || B <= 0 || Hq <= 0 || Hkv <= 0 ||
+        T <= 0 || pos0 < 0 || !(eps >= 0.f) || !std::isfinite(eps) || (k_rot && !table))
+        return GQA_ERR_INVALID_ARG;
+    if (!rope_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(q_out) || (k_out && !aligned16(k_out)) ||
+        (k_rot && !aligned16(k_rot)) || !aligned16(q_gamma) || !aligned16(k_gamma) ||
+        (table && !aligned16(table)))
+        return GQA_ERR_ALIGNMENT;
+    if (k_rot && (long)pos0 + T > (long)table_len) return GQA_ERR_RANGE;
+    return from_cuda(gqa::launch_qk_norm_rope(q, k, q_out, k_out, k_rot, B, Hq, Hkv, T, d, pos0,
+                                              q_gamma, k_gamma, eps, table,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_qk_norm_append(gqa_kv_desc *descs, int nseq, const void *q, const void *k_new,
+                              const void *v_new, int Hq, int Hkv, int d, const float *q_gamma,
+                              const float *k_gamma, float eps, int v_norm, void *q_out,
+                              int32_t *slots_out, gqa_stream_t stream) {
+    if (!descs || !q || !k_new || !v_new || !q_out || !q_gamma || !k_gamma || nseq <= 0 ||
+        Hq <= 0 || Hkv <= 0 || !(eps >= 0.f) || !std::isfinite(eps) ||
+        (v_norm != 0 && v_norm != 1))
+        return GQA_ERR_INVALID_ARG;
+    if (!rope_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(q_out) ||
+        !aligned16(q_gamma) || !aligned16(k_gamma) || (reinterpret_cast<uintptr_t>(descs) & 7u))
+        return GQA_ERR_ALIGNMENT;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    return from_cuda(gqa::launch_qk_norm_append(descs, nseq, q, k_new, v_new, Hq, Hkv, d, q_gamma,
+                                                k_gamma, eps, v_norm, q_out, slots_out, st,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t gqa_decode_workspace_bytes(int nseq, int Hq, int d, int max_len) {
     if (nseq <= 0 || Hq <= 0 || d <= 0 || max_len <= 0) return 0;
     const size_t ns = static_cast<size_t>(gqa::decode_num_splits(max_len));

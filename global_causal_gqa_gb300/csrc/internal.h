@@ -50,6 +50,17 @@ int launch_prefill_wide(const void *q, const void *k_rot, const void *v, void *o
                         int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
                         const float *table, int *status, cudaStream_t s);
 
+// Q/K RMSNorm, K RoPE and cache append (qknorm.cu)
+cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out,
+                                void *k_rot, int B, int Hq, int Hkv, int T, int d, int pos0,
+                                const float *q_gamma, const float *k_gamma, float eps,
+                                const float *table, cudaStream_t s);
+cudaError_t launch_qk_norm_append(gqa_kv_desc *descs, int nseq, const void *q, const void *k_new,
+                                  const void *v_new, int Hq, int Hkv, int d,
+                                  const float *q_gamma, const float *k_gamma, float eps,
+                                  int v_norm, void *q_out, int32_t *slots, int *status,
+                                  cudaStream_t s);
+
 // Bounded-wait self-test (watchdog.cu)
 cudaError_t launch_watchdog_selftest(int64_t limit_ns, int *status, cudaStream_t s);
 

@@ -144,6 +144,36 @@ gqa_status gqa_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new,
                          const void *v_new, int Hkv, int d, int32_t *slots_out,
                          gqa_stream_t stream);
 
+/* ---- Q/K normalisation in front of attention (§3.2, §4.3, §4.4) ----------------------
+ * RMSNorm with an effective gain (§3.2): N(x) = gamma * x / sqrt(mean(x^2) + eps) over
+ * each (token, head) vector of d values; PLaMo's q_norm / k_norm use offset 1, so the
+ * caller passes gamma = 1 + w (the stored weight w plus the offset), eps = 1e-6, and one
+ * gain of d floats shared by every head (§4.3).  The order is fixed by §4.4: normalise,
+ * store K in the cache (normalised, not rotated), then rotate.  Sums of squares and the
+ * scaling run in fp32; each output is rounded once to bf16 (the public implementation's
+ * intermediate bf16 rounding is not reproduced).  d in {64, 128, 256, 512}; gains are
+ * device fp32 [d], 16-byte aligned; outputs may alias their inputs (q_out == q, k_out == k).
+ *
+ * Prefill form: q [B, Hq, T, d] -> q_out = N_q(q) (rotated later, inside
+ * gqa_attn_prefill); k [B, Hkv, T, d] -> k_out = N_k(k) (what the cache stores, nullable)
+ * and k_rot = RoPE(N_k(k)) at positions pos0 + t (nullable; pass it to gqa_attn_prefill
+ * with k_is_rotated = 1).  V is not touched.  table as for gqa_rope_apply; positions
+ * past table_len return GQA_ERR_RANGE. */
+gqa_status gqa_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out, void *k_rot,
+                            int B, int Hq, int Hkv, int T, int d, int pos0,
+                            const float *q_gamma, const float *k_gamma, float eps,
+                            const float *table, int table_len, gqa_stream_t stream);
+
+/* Decode form: for each sequence one new token.  q [nseq, Hq, d] -> q_out = N_q(q) (the
+ * decode kernel rotates it); k_new [nseq, Hkv, d] -> N_k(k_new) and v_new [nseq, Hkv, d]
+ * (unchanged, or with v_norm = 1 normalised without a gain, as Gemma 4 does) are appended
+ * to each sequence's cache exactly as gqa_kv_append appends them (slot, count update,
+ * slots_out, GQA_ERR_CAPACITY on a full linear cache). */
+gqa_status gqa_qk_norm_append(gqa_kv_desc *descs, int nseq, const void *q, const void *k_new,
+                              const void *v_new, int Hq, int Hkv, int d, const float *q_gamma,
+                              const float *k_gamma, float eps, int v_norm, void *q_out,
+                              int32_t *slots_out, gqa_stream_t stream);
+
 /* ---- Decode (§4.4, §4.5) ---------------------------------------------------------------
  * One query token per sequence: q [nseq, Hq, d] bf16 at position R-1, where R = count
  * (linear) or min(count, cap) (ring) read from the descriptors (so call after

@@ -84,6 +84,8 @@ def _load(plant: int = 0) -> ctypes.CDLL:
         lib.orc_allowed_pub.restype = I
         lib.orc_kv_head_pub.argtypes = [I, I, I]
         lib.orc_kv_head_pub.restype = I
+        lib.orc_rms_norm.argtypes = [P, L, I, P, D, P]
+        lib.orc_rms_norm.restype = None
         lib.orc_plant.restype = I
         _LIBS[plant] = lib
         return lib
@@ -136,6 +138,19 @@ class Oracle:
         w = np.ascontiguousarray(w, dtype=np.float64)
         self.lib.orc_rope_rotate(_ptr(y), y.shape[-1], float(pos), _ptr(w), float(amp))
         return y
+
+    # -- RMSNorm ([PL3] §3.2, §4.3) --------------------------------------------------
+    def rms_norm(self, x, gamma, eps: float = 1e-6) -> np.ndarray:
+        """RMSNorm over the last axis of bf16 `x` (tensor or uint16 bits) in fp64;
+        gamma: effective gain [n] (offset + weight) or None for no gain."""
+        xb = _bits(x)
+        n = xb.shape[-1]
+        rows = xb.size // n
+        out = np.zeros(xb.shape, dtype=np.float64)
+        g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float64)
+        self.lib.orc_rms_norm(_ptr(xb), rows, n, None if g is None else _ptr(g), float(eps),
+                              _ptr(out))
+        return out
 
     def allowed(self, qpos: int, kpos: int, window: int) -> bool:
         return bool(self.lib.orc_allowed_pub(qpos, kpos, window))

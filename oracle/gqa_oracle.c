@@ -25,7 +25,9 @@
  *               omega~_j = omega_j [(1 - alpha_j) + alpha_j / s]; amplitude 1 + 0.1 ln s
  *               multiplies both cos and sin;
  *         §6.4  p-RoPE: pairs at or above the rotated fraction get frequency 0 (identity),
- *               the exponent's denominator stays the full head dimension.
+ *               the exponent's denominator stays the full head dimension;
+ *         §3.2, §4.3  RMSNorm with an effective gain (offset + weight), per head for
+ *               q_norm / k_norm (offset 1, eps 1e-6); V is not normalised.
  *   [LLA] disassemble-channel.com LLaMA tutorial, GQA section: g(i) = floor(i n_kv / h),
  *         the same grouping written with the KV-head count.
  *
@@ -125,6 +127,30 @@ void orc_rope_rotate(double *x, int d, double pos, const double *w, double amp) 
         x[j] = a * c - b * s;
         x[j + half] = a * s + b * c;
 #endif
+    }
+}
+
+/* [PL3 §3.2, §4.3] RMSNorm of `rows` vectors of n values (bf16 bits), in double:
+ *   N(x) = gamma (*) x / sqrt((1/n) sum_r x_r^2 + eps)
+ * gamma is the effective gain, offset plus stored weight (q_norm and k_norm: offset 1,
+ * n = head dim, eps = 1e-6, one gain shared by every head); gamma == NULL means no gain
+ * (all ones, the gain-free norm Gemma 4 puts on V).  No mean is subtracted. */
+void orc_rms_norm(const uint16_t *x, long rows, int n, const double *gamma, double eps,
+                  double *out) {
+    for (long i = 0; i < rows; ++i) {
+        const uint16_t *xr = x + (size_t)i * n;
+        double ss = 0.0;
+        for (int r = 0; r < n; ++r) {
+            const double v = bf16_to_f64(xr[r]);
+            ss += v * v;
+        }
+#if ORC_PLANT == 8
+        const double inv = 1.0 / sqrt(ss + eps);       /* planted: sum, not mean */
+#else
+        const double inv = 1.0 / sqrt(ss / n + eps);
+#endif
+        for (int r = 0; r < n; ++r)
+            out[(size_t)i * n + r] = (gamma ? gamma[r] : 1.0) * bf16_to_f64(xr[r]) * inv;
     }
 }
 

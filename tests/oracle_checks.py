@@ -349,7 +349,46 @@ def check_ring_equals_full_history(orc):
         assert np.max(np.abs(of[0, :, n_before] - o[0])) < 1e-9, n_before
 
 
+# ---------------------------------------------------------------------------------
+# RMSNorm with an effective gain (PLaMo page §3.2 formula, §4.3 q_norm / k_norm)
+# ---------------------------------------------------------------------------------
+
+def check_rms_norm_closed_form(orc):
+    """A constant vector a*1 normalises to gamma * a / sqrt(a^2 + eps) in every
+    component; with eps = 0 any vector's normalised mean square (gain 1) is exactly 1."""
+    n, a, eps = 128, 2.0, 1e-6
+    x = torch.full((2, n), a).to(torch.bfloat16)
+    gamma = 1.0 + np.linspace(-0.25, 0.5, n)          # offset 1 plus a stored weight
+    y = orc.rms_norm(x, gamma, eps)
+    want = gamma * a / math.sqrt(a * a + eps)
+    assert np.max(np.abs(y - want[None, :])) < 1e-12, np.max(np.abs(y - want))
+    z = orc.rms_norm(_bf16((5, 96), 501), None, 0.0)
+    assert np.max(np.abs(np.mean(z * z, axis=-1) - 1.0)) < 1e-12
+
+
+def check_rms_norm_library(orc):
+    """torch.nn.functional.rms_norm in fp64 with the effective gain as its weight."""
+    x = _bf16((7, 3, 128), 502)
+    gamma = 1.0 + 0.1 * _f64(_bf16((128,), 503))
+    y = orc.rms_norm(x, gamma, 1e-6)
+    ref = torch.nn.functional.rms_norm(x.to(torch.float64), (128,),
+                                       weight=torch.from_numpy(gamma), eps=1e-6).numpy()
+    assert np.max(np.abs(y - ref)) < 1e-12, np.max(np.abs(y - ref))
+
+
+def check_rms_norm_scale_invariance(orc):
+    """N(4x) = N(x) up to the epsilon term (4x is exact in bf16)."""
+    x = _bf16((6, 128), 504)
+    x4 = (x.to(torch.float32) * 4).to(torch.bfloat16)
+    a = orc.rms_norm(x, None, 1e-6)
+    b = orc.rms_norm(x4, None, 1e-6)
+    assert np.max(np.abs(a - b)) < 1e-5, np.max(np.abs(a - b))
+
+
 ALL_CHECKS = [
+    check_rms_norm_closed_form,
+    check_rms_norm_library,
+    check_rms_norm_scale_invariance,
     check_worked_example,
     check_yarn_constants,
     check_yarn_curve,

@@ -84,3 +84,23 @@ def test_watchdog_selftest_limits_rejected_on_host():
     S = gqa.STATUS_NAMES
     for bad in (0, 999, -5, 2_000_000_001):
         assert S[L.gqa_watchdog_selftest(bad, None)] == "GQA_ERR_INVALID_ARG", bad
+
+
+def test_qk_norm_arguments_rejected_on_host():
+    L = gqa.lib()
+    S = gqa.STATUS_NAMES
+    f = lambda st: S.get(st, st)  # noqa: E731
+    fake = 0x10000
+    # null gain, unsupported d, misaligned output, position past the table, bad v_norm
+    assert f(L.gqa_qk_norm_rope(fake, fake, fake, None, None, 1, 2, 1, 8, 128, 0, None, fake,
+                                1e-6, None, 0, None)) == "GQA_ERR_INVALID_ARG"
+    assert f(L.gqa_qk_norm_rope(fake, fake, fake, None, None, 1, 2, 1, 8, 96, 0, fake, fake,
+                                1e-6, None, 0, None)) == "GQA_ERR_UNSUPPORTED"
+    assert f(L.gqa_qk_norm_rope(fake, fake, fake + 4, None, None, 1, 2, 1, 8, 128, 0, fake,
+                                fake, 1e-6, None, 0, None)) == "GQA_ERR_ALIGNMENT"
+    assert f(L.gqa_qk_norm_rope(fake, fake, fake, None, fake, 1, 2, 1, 8, 128, 3, fake, fake,
+                                1e-6, fake, 10, None)) == "GQA_ERR_RANGE"
+    assert f(L.gqa_qk_norm_append(fake, 1, fake, fake, fake, 2, 1, 128, fake, fake, 1e-6, 2,
+                                  fake, None, None)) == "GQA_ERR_INVALID_ARG"
+    assert f(L.gqa_qk_norm_append(fake, 1, fake, fake, fake, 2, 1, 128, fake, fake, -1.0, 0,
+                                  fake, None, None)) == "GQA_ERR_INVALID_ARG"
