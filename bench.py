@@ -650,7 +650,7 @@ def main():
     extra = []
     if world == 1 and not args.no_extra:
         for name in ("plamo3_local_prefill", "plamo3_global_prefill", "plamo3_decode_batch32",
-                     "gemma4_period_6layer"):
+                     "gemma4_period_6layer", "gemma4_decode_global", "gemma4_decode_local"):
             if name == wl.name:
                 continue
             other = get_workload(name)

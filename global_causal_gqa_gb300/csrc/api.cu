@@ -226,7 +226,7 @@ gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, in
     if (!q || !descs || !o || nseq <= 0 || Hq <= 0 || Hkv <= 0 || (Hq % Hkv) != 0 ||
         max_len <= 0 || !std::isfinite(scale))
         return GQA_ERR_INVALID_ARG;
-    if (d != 128 || Hq / Hkv > 8) return GQA_ERR_UNSUPPORTED;
+    if ((d != 128 && d != 256 && d != 512) || Hq / Hkv > 8) return GQA_ERR_UNSUPPORTED;
     if (nseq > 65535) return GQA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(o) || (reinterpret_cast<uintptr_t>(descs) & 7u) ||
         (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
@@ -274,7 +274,7 @@ gqa_status gqa_attn_decode_static(const void *q, const gqa_kv_desc *descs, int n
     if (!q || !descs || !o || nseq <= 0 || Hq <= 0 || Hkv <= 0 || (Hq % Hkv) != 0 ||
         max_len <= 0 || !std::isfinite(scale))
         return GQA_ERR_INVALID_ARG;
-    if (d != 128 || Hq / Hkv > 8) return GQA_ERR_UNSUPPORTED;
+    if ((d != 128 && d != 256 && d != 512) || Hq / Hkv > 8) return GQA_ERR_UNSUPPORTED;
     if (nseq > 65535) return GQA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(o) || (reinterpret_cast<uintptr_t>(descs) & 7u) ||
         (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))

@@ -5,9 +5,15 @@
 // §4.5 (attention equation), §2.3 (decode reads every cached K and V once per step:
 // 4 Hkv d bytes per token and layer -- the bound this kernel is written against).
 //
-// Work split: one CTA per (split of kDecodeChunk keys, sequence, block of <= 8 KV heads);
-// one warp per KV head streams its keys in blocks of 16 with 16-byte read-only loads,
-// double-buffered in registers so the next block's loads are in flight during the math.
+// Work split: one CTA per (split of decode_chunk(max_len) keys, sequence, block of KV
+// heads); each
+// KV head is streamed by d/128 warps (d = 128, 256, 512), each of which owns the pairs
+// [64 p, 64 p + 64) of the split-half RoPE -- head-dim elements 64p.. and d/2 + 64p.. -- so
+// every warp sees a 128-element vector whose RoPE pairs are (l, l + 64), the d = 128
+// layout.  Keys go in blocks of 16 with 16-byte read-only loads, double-buffered in
+// registers so the next block's loads are in flight during the math; the warps of a
+// head add their partial scores through shared memory (one named barrier per block)
+// and each accumulates the output for its own elements.
 // The query group of G <= 8 heads shares every K and V element, so the per-block math
 // is two warp-level bf16 MMAs (m16n8k16): S^T = K' Q'^T and O^T += V^T P^T, fp32
 // accumulate.  The head dimension is permuted (identically on both operands of each
@@ -27,7 +33,8 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kWarps = 8;
-constexpr int kDecodeSmem = kWarps * 2 * 512 * 16;   // two 8 KB table stages per warp
+// two 8 KB table stages per warp, then the partial-score exchange (8 KB)
+constexpr int kDecodeSmem = kWarps * 2 * 512 * 16 + kWarps * 2 * 32 * 4 * 4;
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -122,14 +129,22 @@ __device__ __forceinline__ SeqView seq_view(const gqa_kv_desc &desc, int max_len
     return v;
 }
 
+template <int PARTS>   // warps per KV head: d = 128 PARTS
 __global__ void __launch_bounds__(kWarps * 32, 1)
     decode_partial_kernel(const __nv_bfloat16 *__restrict__ q,
                           const gqa_kv_desc *__restrict__ descs, int Hq, int Hkv,
                           float scale_log2, int max_len, int nsplit, float *__restrict__ ws_ml,
                           float *__restrict__ ws_o, int *status) {
+    constexpr int d = kD * PARTS, parts = PARTS;
     const int split = blockIdx.x, seq = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = blockIdx.z * kWarps + warp;
+    const int part = warp % parts;               // this warp's RoPE pairs: [64 part, +64)
+    const int hg = warp / parts;                 // head group within the CTA
+    const int g = blockIdx.z * (kWarps / parts) + hg;
+    // global 16-byte chunk of the row for local chunk lc (8 elements) of this warp
+    auto gchunk = [&](int lc) {
+        return lc < 8 ? 8 * part + lc : d / 16 + 8 * part + (lc - 8);
+    };
     const gqa_kv_desc desc = descs[seq];
     const SeqView sv = seq_view(desc, max_len);
     if (!sv.ok) {
@@ -138,9 +153,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                                                                    : GQA_ERR_RANGE);
         return;
     }
-    const int k_start = split * kDecodeChunk;
+    const int chunk = decode_chunk(max_len);
+    const int k_start = split * chunk;
     if (k_start >= sv.R || g >= Hkv) return;
-    const int k_end = min(sv.R, k_start + kDecodeChunk);
+    const int k_end = min(sv.R, k_start + chunk);
     const int G = Hq / Hkv;
     const int qpos = sv.R - 1;
     const int gq = lane >> 2, tq = lane & 3;
@@ -153,12 +169,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         uint4 qc[4];
         if (gq < G) {
             const uint4 *qr = reinterpret_cast<const uint4 *>(
-                q + ((size_t)seq * Hq + (size_t)g * G + gq) * kD);
+                q + ((size_t)seq * Hq + (size_t)g * G + gq) * d);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) qc[c] = qr[4 * c + tq];
+            for (int c = 0; c < 4; ++c) qc[c] = qr[gchunk(4 * c + tq)];
 #pragma unroll
             for (int c = 0; c < 2; ++c)
-                rotate8(qc[c], qc[c + 2], table + (size_t)qpos * (kD / 2) + 32 * c + 8 * tq);
+                rotate8(qc[c], qc[c + 2],
+                        table + (size_t)qpos * (d / 2) + 64 * part + 32 * c + 8 * tq);
         } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c) qc[c] = make_uint4(0, 0, 0, 0);
@@ -183,9 +200,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     // The XOR keeps both the copies in and the reads out free of bank conflicts.
     extern __shared__ float4 dsmem[];
     float4 *stage_base = dsmem + (size_t)warp * 2 * 512;
+    float *xchg = reinterpret_cast<float *>(dsmem + (size_t)kWarps * 2 * 512) +
+                  (size_t)hg * (2 * parts * 32 * 4);
 
-    const __nv_bfloat16 *kbase = static_cast<const __nv_bfloat16 *>(desc.k) + (size_t)g * sv.cap * kD;
-    const __nv_bfloat16 *vbase = static_cast<const __nv_bfloat16 *>(desc.v) + (size_t)g * sv.cap * kD;
+    const __nv_bfloat16 *kbase = static_cast<const __nv_bfloat16 *>(desc.k) + (size_t)g * sv.cap * d;
+    const __nv_bfloat16 *vbase = static_cast<const __nv_bfloat16 *>(desc.v) + (size_t)g * sv.cap * d;
     auto slot_of = [&](int key) {
         int s = sv.first + key;
         return s >= sv.cap ? s - sv.cap : s;
@@ -204,19 +223,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     auto load = [&](Block &bl, int kb) {
         bl.kb = kb;
         const int kk0 = min(kb + gq, k_end - 1), kk1 = min(kb + gq + 8, k_end - 1);
-        const uint4 *kr0 = reinterpret_cast<const uint4 *>(kbase + (size_t)slot_of(kk0) * kD);
-        const uint4 *kr1 = reinterpret_cast<const uint4 *>(kbase + (size_t)slot_of(kk1) * kD);
+        const uint4 *kr0 = reinterpret_cast<const uint4 *>(kbase + (size_t)slot_of(kk0) * d);
+        const uint4 *kr1 = reinterpret_cast<const uint4 *>(kbase + (size_t)slot_of(kk1) * d);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            bl.k0[c] = ld_stream(kr0 + 4 * c + tq);
-            bl.k1[c] = ld_stream(kr1 + 4 * c + tq);
+            bl.k0[c] = ld_stream(kr0 + gchunk(4 * c + tq));
+            bl.k1[c] = ld_stream(kr1 + gchunk(4 * c + tq));
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int key = min(kb + 2 * tq + (i & 1) + ((i >> 1) << 3), k_end - 1);
-            const uint4 *vr = reinterpret_cast<const uint4 *>(vbase + (size_t)slot_of(key) * kD);
-            bl.vv[i][0] = ld_stream(vr + gq);
-            bl.vv[i][1] = ld_stream(vr + 8 + gq);
+            const uint4 *vr = reinterpret_cast<const uint4 *>(vbase + (size_t)slot_of(key) * d);
+            bl.vv[i][0] = ld_stream(vr + gchunk(gq));
+            bl.vv[i][1] = ld_stream(vr + gchunk(8 + gq));
         }
         // table rows kb .. kb + 15: instruction i copies row i (clamped), lane = 16-byte
         // piece of the row, i.e. pairs 2 lane, 2 lane + 1 = 32c + 8tq + 2qq
@@ -230,7 +249,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             const int k = ((i >> 3) << 3) | kq;
             const int lp = ((i & 7) << 2) | lp_lo;
             cp_async16(stg + k * 32 + (lp ^ ((k & 3) << 1)),
-                       reinterpret_cast<const float4 *>(table + (size_t)row * (kD / 2)) + lane);
+                       reinterpret_cast<const float4 *>(table + (size_t)row * (d / 2) +
+                                                        64 * part) + lane);
         }
         cp_async_commit();
     };
@@ -263,6 +283,24 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) s[i] += t[i];
+        if constexpr (PARTS > 1) {
+            // add the other warps' partial scores for the same (key, head) fragment
+            float *xb = xchg + (size_t)(((kb - k_start) >> 4) & 1) * (parts * 128);
+            reinterpret_cast<float4 *>(xb + part * 128)[lane] = make_float4(s[0], s[1], s[2], s[3]);
+            named_bar_sync(1 + hg, 32 * parts);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int pp = 0; pp < parts; ++pp) {
+                const float4 v = reinterpret_cast<const float4 *>(xb + pp * 128)[lane];
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            s[0] = acc.x;
+            s[1] = acc.y;
+            s[2] = acc.z;
+            s[3] = acc.w;
+        }
         // online softmax per head column (heads 2tq, 2tq+1), log2 domain
         const float x0 = ok0 ? s[0] * scale_log2 : -CUDART_INF_F;
         const float x1 = ok0 ? s[1] * scale_log2 : -CUDART_INF_F;
@@ -320,38 +358,44 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const int h0 = 2 * tq, h1 = 2 * tq + 1;  // heads within the group
     const size_t rec0 = ((size_t)seq * Hq + (size_t)g * G + h0) * nsplit + split;
     const size_t rec1 = ((size_t)seq * Hq + (size_t)g * G + h1) * nsplit + split;
+    // this warp's output elements: local 64 (i >> 1) + 8 gq + 4 (i & 1) + 0..3, i.e.
+    // global 64 part + 8 gq + ... in the first half and d/2 + 64 part + ... in the second
+    auto out_off = [&](int i) {
+        return (i >> 1) * (d / 2) + 64 * part + 8 * gq + 4 * (i & 1);
+    };
     if (h0 < G) {
-        if (gq == 0) {
+        if (gq == 0 && part == 0) {
             ws_ml[2 * rec0] = m_run0;
             ws_ml[2 * rec0 + 1] = l_run0;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            reinterpret_cast<float4 *>(ws_o + rec0 * kD + 64 * (i >> 1) + 8 * gq)[i & 1] =
+            *reinterpret_cast<float4 *>(ws_o + rec0 * d + out_off(i)) =
                 make_float4(o[2 * i][0], o[2 * i][2], o[2 * i + 1][0], o[2 * i + 1][2]);
     }
     if (h1 < G) {
-        if (gq == 0) {
+        if (gq == 0 && part == 0) {
             ws_ml[2 * rec1] = m_run1;
             ws_ml[2 * rec1 + 1] = l_run1;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            reinterpret_cast<float4 *>(ws_o + rec1 * kD + 64 * (i >> 1) + 8 * gq)[i & 1] =
+            *reinterpret_cast<float4 *>(ws_o + rec1 * d + out_off(i)) =
                 make_float4(o[2 * i][1], o[2 * i][3], o[2 * i + 1][1], o[2 * i + 1][3]);
     }
 }
 
 // One block per (query head, sequence), one thread per head-dim element.
-__global__ void __launch_bounds__(kD)
-    decode_combine_kernel(const gqa_kv_desc *__restrict__ descs, int Hq, int max_len,
+__global__ void __launch_bounds__(kMaxHeadDim)
+    decode_combine_kernel(const gqa_kv_desc *__restrict__ descs, int Hq, int d, int max_len,
                           int nsplit, const float *__restrict__ ws_ml,
                           const float *__restrict__ ws_o, __nv_bfloat16 *__restrict__ out,
                           float *__restrict__ lse) {
     const int h = blockIdx.x, seq = blockIdx.y, dd = threadIdx.x;
     const SeqView sv = seq_view(descs[seq], max_len);
     if (!sv.ok) return;
-    const int ns = (sv.R + kDecodeChunk - 1) / kDecodeChunk;
+    const int chunk = decode_chunk(max_len);
+    const int ns = (sv.R + chunk - 1) / chunk;
     const size_t rec = ((size_t)seq * Hq + h) * nsplit;
     float M = -CUDART_INF_F;
     for (int s = 0; s < ns; ++s) M = fmaxf(M, ws_ml[2 * (rec + s)]);
@@ -359,41 +403,50 @@ __global__ void __launch_bounds__(kD)
     for (int s = 0; s < ns; ++s) {
         const float f = ex2_approx(ws_ml[2 * (rec + s)] - M);
         L += ws_ml[2 * (rec + s) + 1] * f;
-        acc += ws_o[(rec + s) * kD + dd] * f;
+        acc += ws_o[(rec + s) * d + dd] * f;
     }
-    out[((size_t)seq * Hq + h) * kD + dd] = __float2bfloat16_rn(acc / L);
+    out[((size_t)seq * Hq + h) * d + dd] = __float2bfloat16_rn(acc / L);
     if (lse && dd == 0) lse[(size_t)seq * Hq + h] = (M + __log2f(L)) * 0.69314718055994531f;
 }
 
 }  // namespace
 
-int decode_num_splits(int max_len) { return (max_len + kDecodeChunk - 1) / kDecodeChunk; }
+int decode_num_splits(int max_len) {
+    return (max_len + decode_chunk(max_len) - 1) / decode_chunk(max_len);
+}
 
 cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
                           int d, float scale, int max_len, void *o, float *lse, float *ws,
                           int *status, cudaStream_t s) {
-    (void)d;
     const int nsplit = decode_num_splits(max_len);
     float *ws_ml = ws;
     float *ws_o = ws + (size_t)2 * nseq * Hq * nsplit;
-    const int warps = Hkv < kWarps ? Hkv : kWarps;
-    dim3 grid(nsplit, nseq, (Hkv + kWarps - 1) / kWarps);
+    const int parts = d / kD;                       // warps per KV head
+    const int heads_per_cta = kWarps / parts;
+    const int heads = Hkv < heads_per_cta ? Hkv : heads_per_cta;
+    dim3 grid(nsplit, nseq, (Hkv + heads_per_cta - 1) / heads_per_cta);
     const float scale_log2 = scale * 1.4426950408889634f;
     static bool attr_done = false;
     if (!attr_done) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            decode_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
-        if (e != cudaSuccess) return e;
+        for (const void *f : {reinterpret_cast<const void *>(decode_partial_kernel<1>),
+                              reinterpret_cast<const void *>(decode_partial_kernel<2>),
+                              reinterpret_cast<const void *>(decode_partial_kernel<4>)}) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+            if (e != cudaSuccess) return e;
+        }
         attr_done = true;
     }
-    decode_partial_kernel<<<grid, warps * 32, warps * 2 * 512 * sizeof(float4), s>>>(
+    auto kern = parts == 1 ? decode_partial_kernel<1>
+                : parts == 2 ? decode_partial_kernel<2> : decode_partial_kernel<4>;
+    kern<<<grid, heads * parts * 32, kDecodeSmem, s>>>(
         static_cast<const __nv_bfloat16 *>(q), descs, Hq, Hkv, scale_log2, max_len, nsplit,
         ws_ml, ws_o, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<<<dim3(Hq, nseq), kD, 0, s>>>(descs, Hq, max_len, nsplit, ws_ml,
-                                                         ws_o, static_cast<__nv_bfloat16 *>(o),
-                                                         lse);
+    decode_combine_kernel<<<dim3(Hq, nseq), d, 0, s>>>(descs, Hq, d, max_len, nsplit, ws_ml,
+                                                        ws_o, static_cast<__nv_bfloat16 *>(o),
+                                                        lse);
     return cudaGetLastError();
 }
 

@@ -25,10 +25,13 @@ cudaError_t launch_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new,
                              int *status, cudaStream_t s);
 
 // Decode (decode.cu)
-#ifndef GQA_DECODE_CHUNK
-#define GQA_DECODE_CHUNK 1024
-#endif
-constexpr int kDecodeChunk = GQA_DECODE_CHUNK;  // keys per split
+// Keys per split: 1024 for long caches; 256 when max_len <= 4096, so that short caches
+// (a local layer's ring of a few thousand tokens) still give enough CTAs to fill the GPU.
+constexpr int kDecodeChunkLong = 1024;
+constexpr int kDecodeChunkShort = 256;
+__host__ __device__ inline int decode_chunk(int max_len) {
+    return max_len > 4096 ? kDecodeChunkLong : kDecodeChunkShort;
+}
 int decode_num_splits(int max_len);
 cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
                           int d, float scale, int max_len, void *o, float *lse,

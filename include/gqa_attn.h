@@ -27,9 +27,9 @@
  *   - Errors found on the device (a bounded wait that expired, a full cache, an index
  *     out of range) are recorded in the device status word and returned by the next
  *     gqa_get_device_status().  Device code never traps.
- *   - Head dims: prefill d in {128, 256, 512}; decode d = 128; kv_append and rope_apply d in
- *     {64, 128, 256, 512}.  Query group G = Hq/Hkv must be an integer; decode needs
- *     G <= 8.  Other values return GQA_ERR_UNSUPPORTED.
+ *   - Head dims: prefill and decode d in {128, 256, 512}; kv_append, rope_apply and the
+ *     Q/K normalisation d in {64, 128, 256, 512}.  Query group G = Hq/Hkv must be an
+ *     integer; decode needs G <= 8.  Other values return GQA_ERR_UNSUPPORTED.
  */
 #ifndef GQA_ATTN_H
 #define GQA_ATTN_H
@@ -181,8 +181,10 @@ gqa_status gqa_qk_norm_append(gqa_kv_desc *descs, int nseq, const void *q, const
  * with the sequence's table.  o: [nseq, Hq, d] bf16; lse: [nseq, Hq] float or NULL.
  * max_len: an upper bound on R over the batch (sizes the split-KV grid); a sequence with
  * R > max_len or rope_len < R is skipped and flagged in the status word.
- * workspace: device scratch of gqa_decode_workspace_bytes(nseq, Hq, d, max_len) bytes.
- * d = 128, Hq/Hkv <= 16. */
+ * workspace: device scratch of gqa_decode_workspace_bytes(nseq, Hq, d, max_len) bytes:
+ * nseq Hq nsplit (d + 2) floats of split partials, nsplit = ceil(max_len / chunk) with
+ * chunk = 1024 keys when max_len > 4096 and 256 otherwise.
+ * d in {128, 256, 512} (Gemma-4 local / global heads), Hq/Hkv <= 8. */
 size_t gqa_decode_workspace_bytes(int nseq, int Hq, int d, int max_len);
 gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq,
                            int Hkv, int d, float scale, int max_len, void *o, float *lse,

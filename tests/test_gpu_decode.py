@@ -166,3 +166,27 @@ def test_plamo3_decode_batch_full_size():
     assert np.array_equal(st.counts(), rcounts)
     gu.compare(o, ro, what="plamo3 decode")
     gu.compare(lse, rl, what="plamo3 decode lse")
+
+
+PROPE = RopeSpec(base=1e6, rotate_fraction=0.25)
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(16, 8, 256), (16, 2, 512), (8, 1, 256), (32, 4, 512),
+                                      (6, 3, 256)])
+def test_wide_head_decode(Hq, Hkv, d):
+    """Gemma-4 head dims: d = 256 (local layers) and 512 (global), streamed by 2 or 4 warps
+    per KV head; linear caches across split boundaries and rings around wrap-around."""
+    gu.require_gpu()
+    lengths = [0, 15, 1023, 1024, 2100]
+    rings = [(64, 10), (64, 200), (1024, 1023), (1024, 3000)]
+    x = _random_batch(lengths, rings, Hq, Hkv, d, seed=Hq + Hkv + d)
+    if d == 512:
+        x = replace(x, rope=[PROPE if not r else LOCAL for r in x.is_ring])
+    st = DecodeSetup(x, d)
+    scale = 1 / math.sqrt(d)
+    o, lse, slots = run_step(st, Hq, Hkv, scale, max_len=4096)
+    ro, rl, rslots, rcounts = oracle_step(x, d, scale)
+    assert np.array_equal(slots.cpu().numpy().astype(np.int64), rslots)
+    assert np.array_equal(st.counts(), rcounts)
+    gu.compare(o, ro, what=f"decode d={d} Hq={Hq} Hkv={Hkv}")
+    gu.compare(lse, rl, what="decode lse")

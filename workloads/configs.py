@@ -114,8 +114,21 @@ GEMMA4_PERIOD = PrefillWorkload("gemma4_period_6layer", tuple(
     [PrefillLayer(B=1, T=16384, S=16384, Hq=16, Hkv=2, d=512, window=0,
                   rope=_G4_GLOBAL, scale=1 / math.sqrt(512), seed=5010)]))
 
+# Gemma-4-shaped decode batches (one head shape per call): the global layer's d = 512,
+# 2 KV heads and p-RoPE over linear caches, and the local layers' d = 256, 8 KV heads over
+# rings of the 1024-token window.  Lengths as in the PLaMo decode batch.
+GEMMA4_DECODE_GLOBAL = DecodeWorkload(
+    "gemma4_decode_global", n_global=32, n_local=0, Hq=16, Hkv=2, d=512,
+    global_len_range=(8192, 65536), window=1024, rope_global=_G4_GLOBAL,
+    rope_local=_G4_LOCAL, scale=1 / math.sqrt(512), seed=6006)
+GEMMA4_DECODE_LOCAL = DecodeWorkload(
+    "gemma4_decode_local", n_global=0, n_local=32, Hq=16, Hkv=8, d=256,
+    global_len_range=(1024, 1024), window=1024, rope_global=_G4_GLOBAL,
+    rope_local=_G4_LOCAL, scale=1 / math.sqrt(256), seed=7007)
+
 WORKLOADS = {w.name: w for w in (TINY_W64, TINY_CAUSAL, PLAMO3_LOCAL_PREFILL,
-                                 PLAMO3_GLOBAL_PREFILL, PLAMO3_DECODE, GEMMA4_PERIOD)}
+                                 PLAMO3_GLOBAL_PREFILL, PLAMO3_DECODE, GEMMA4_PERIOD,
+                                 GEMMA4_DECODE_GLOBAL, GEMMA4_DECODE_LOCAL)}
 
 
 def get_workload(name: str):
