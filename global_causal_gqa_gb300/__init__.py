@@ -24,7 +24,7 @@ __all__ = [
     "gqa_rope_inv_freq", "gqa_yarn_amplitude", "gqa_rope_table_bytes", "gqa_rope_table_build",
     "gqa_rope_apply", "gqa_prefill_workspace_bytes", "gqa_attn_prefill", "gqa_kv_append",
     "gqa_decode_workspace_bytes", "gqa_attn_decode", "gqa_attn_decode_static",
-    "gqa_qk_norm_rope", "gqa_qk_norm_append",
+    "gqa_qk_norm_rope", "gqa_qk_norm_append", "gqa_prefill_gather", "gqa_kv_append_chunk",
     "gqa_get_device_status", "gqa_get_device_diag", "gqa_watchdog_selftest",
     "gqa_status_string", "gqa_last_error_string", "gqa_device_check",
 ]
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
             "gqa_decode_workspace_bytes": ([I, I, I, I], Z),
             "gqa_attn_decode": ([P, P, I, I, I, I, F, I, P, P, P, Z, P], I),
             "gqa_attn_decode_static": ([P, P, I, I, I, I, F, I, P, P, P], I),
+            "gqa_prefill_gather": ([P, P, P, I, I, I, P, P, I, P, I, P], I),
+            "gqa_kv_append_chunk": ([P, I, P, P, I, I, I, P], I),
             "gqa_qk_norm_rope": ([P, P, P, P, P, I, I, I, I, I, I, P, P, F, P, I, P], I),
             "gqa_qk_norm_append": ([P, I, P, P, P, I, I, I, P, P, F, I, P, P, P], I),
             "gqa_get_device_status": ([P], I),
@@ -215,6 +217,22 @@ def gqa_attn_decode_static(q, descs, nseq: int, Hq: int, Hkv: int, d: int, scale
     st = lib().gqa_attn_decode_static(_ptr(q), _ptr(descs), nseq, Hq, Hkv, d, scale, max_len,
                                       _ptr(o), _ptr(lse), _stream(stream))
     return _check("gqa_attn_decode_static", st, check)
+
+
+# ---- chunked prefill over a cache -------------------------------------------------------------
+
+def gqa_prefill_gather(desc, k_new, v_new, T: int, Hkv: int, d: int, k_out, v_out, S: int,
+                       table, table_len: int, stream=None, check: bool = True) -> int:
+    st = lib().gqa_prefill_gather(_ptr(desc), _ptr(k_new), _ptr(v_new), T, Hkv, d, _ptr(k_out),
+                                  _ptr(v_out), S, _ptr(table), table_len, _stream(stream))
+    return _check("gqa_prefill_gather", st, check)
+
+
+def gqa_kv_append_chunk(descs, nseq: int, k_new, v_new, T: int, Hkv: int, d: int, stream=None,
+                        check: bool = True) -> int:
+    st = lib().gqa_kv_append_chunk(_ptr(descs), nseq, _ptr(k_new), _ptr(v_new), T, Hkv, d,
+                                   _stream(stream))
+    return _check("gqa_kv_append_chunk", st, check)
 
 
 # ---- Q/K normalisation ------------------------------------------------------------------------

@@ -177,6 +177,37 @@ gqa_status gqa_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new, const 
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
+gqa_status gqa_prefill_gather(const gqa_kv_desc *desc, const void *k_new, const void *v_new,
+                              int T, int Hkv, int d, void *k_out, void *v_out, int S,
+                              const float *table, int table_len, gqa_stream_t stream) {
+    if (!desc || !k_new || !v_new || !k_out || !v_out || !table || T <= 0 || Hkv <= 0 ||
+        S < T || table_len <= 0)
+        return GQA_ERR_INVALID_ARG;
+    if (!rope_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_out) || !aligned16(v_out) ||
+        !aligned16(table) || (reinterpret_cast<uintptr_t>(desc) & 7u))
+        return GQA_ERR_ALIGNMENT;
+    if (S > table_len) return GQA_ERR_RANGE;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    return from_cuda(gqa::launch_prefill_gather(desc, k_new, v_new, T, Hkv, d, k_out, v_out, S,
+                                                table, table_len, st,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_kv_append_chunk(gqa_kv_desc *descs, int nseq, const void *k_new,
+                               const void *v_new, int T, int Hkv, int d, gqa_stream_t stream) {
+    if (!descs || !k_new || !v_new || nseq <= 0 || T <= 0 || Hkv <= 0)
+        return GQA_ERR_INVALID_ARG;
+    if (!rope_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
+    if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(descs) & 7u))
+        return GQA_ERR_ALIGNMENT;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    return from_cuda(gqa::launch_kv_append_chunk(descs, nseq, k_new, v_new, T, Hkv, d, st,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 gqa_status gqa_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out, void *k_rot,
                             int B, int Hq, int Hkv, int T, int d, int pos0,
                             const float *q_gamma, const float *k_gamma, float eps,

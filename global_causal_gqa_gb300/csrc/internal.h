@@ -53,6 +53,15 @@ int launch_prefill_wide(const void *q, const void *k_rot, const void *v, void *o
                         int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
                         const float *table, int *status, cudaStream_t s);
 
+// Chunked prefill over a cache (chunk.cu)
+cudaError_t launch_prefill_gather(const gqa_kv_desc *desc, const void *k_new, const void *v_new,
+                                  int T, int Hkv, int d, void *k_out, void *v_out, int S,
+                                  const float *table, int table_len, int *status,
+                                  cudaStream_t s);
+cudaError_t launch_kv_append_chunk(gqa_kv_desc *descs, int nseq, const void *k_new,
+                                   const void *v_new, int T, int Hkv, int d, int *status,
+                                   cudaStream_t s);
+
 // Q/K RMSNorm, K RoPE and cache append (qknorm.cu)
 cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out,
                                 void *k_rot, int B, int Hq, int Hkv, int T, int d, int pos0,

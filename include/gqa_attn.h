@@ -144,6 +144,30 @@ gqa_status gqa_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new,
                          const void *v_new, int Hkv, int d, int32_t *slots_out,
                          gqa_stream_t stream);
 
+/* ---- Chunked prefill over a cache (§4.4) ----------------------------------------------
+ * A chunk of T new tokens of one sequence attends to the R tokens its cache holds
+ * (linear: R = count; ring: R = min(count, cap), the newest ones, oldest first) followed
+ * by itself: S = R + T keys at positions 0..S-1 and queries at R..S-1 (a local layer's
+ * ring is re-numbered from 0, §4.4; its window W = cap covers every key a chunk query can
+ * see).  Per chunk: gqa_prefill_gather, then gqa_attn_prefill(q [1, Hq, T, d], k_out,
+ * v_out, B = 1, T, S, ..., k_is_rotated = 1), then gqa_kv_append_chunk.
+ *
+ * gqa_prefill_gather: desc is one device descriptor; k_new, v_new [Hkv, T, d] are the
+ * chunk's keys (before RoPE) and values; k_out, v_out [Hkv, S, d] (caller-owned) receive
+ * the S keys rotated at positions 0..S-1 and the S values.  S is the caller's count of
+ * R + T; if the descriptor disagrees, or S > table_len, nothing is written and the status
+ * word records GQA_ERR_CAPACITY (resp. GQA_ERR_RANGE).
+ *
+ * gqa_kv_append_chunk: k_new, v_new [nseq, Hkv, T, d]; each sequence's T tokens go to slots
+ * count .. count + T - 1 (linear; if they do not fit, nothing is written and the status
+ * word records GQA_ERR_CAPACITY) or (count + t) mod cap (ring; when T > cap only the last
+ * cap tokens are stored), then count += T.  d in {64, 128, 256, 512}. */
+gqa_status gqa_prefill_gather(const gqa_kv_desc *desc, const void *k_new, const void *v_new,
+                              int T, int Hkv, int d, void *k_out, void *v_out, int S,
+                              const float *table, int table_len, gqa_stream_t stream);
+gqa_status gqa_kv_append_chunk(gqa_kv_desc *descs, int nseq, const void *k_new,
+                               const void *v_new, int T, int Hkv, int d, gqa_stream_t stream);
+
 /* ---- Q/K normalisation in front of attention (§3.2, §4.3, §4.4) ----------------------
  * RMSNorm with an effective gain (§3.2): N(x) = gamma * x / sqrt(mean(x^2) + eps) over
  * each (token, head) vector of d values; PLaMo's q_norm / k_norm use offset 1, so the

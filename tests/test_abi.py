@@ -107,3 +107,21 @@ def test_qk_norm_arguments_rejected_on_host():
                                   fake, None, None)) == "GQA_ERR_INVALID_ARG"
     assert f(L.gqa_qk_norm_append(fake, 1, fake, fake, fake, 2, 1, 128, fake, fake, -1.0, 0,
                                   fake, None, None)) == "GQA_ERR_INVALID_ARG"
+
+
+def test_chunked_prefill_arguments_rejected_on_host():
+    L = gqa.lib()
+    S = gqa.STATUS_NAMES
+    f = lambda st: S.get(st, st)  # noqa: E731
+    fake = 0x10000
+    # S < T, unsupported d, misaligned output, S past the table
+    assert f(L.gqa_prefill_gather(fake, fake, fake, 8, 1, 128, fake, fake, 4, fake, 64,
+                                  None)) == "GQA_ERR_INVALID_ARG"
+    assert f(L.gqa_prefill_gather(fake, fake, fake, 8, 1, 96, fake, fake, 16, fake, 64,
+                                  None)) == "GQA_ERR_UNSUPPORTED"
+    assert f(L.gqa_prefill_gather(fake, fake, fake, 8, 1, 128, fake + 8, fake, 16, fake, 64,
+                                  None)) == "GQA_ERR_ALIGNMENT"
+    assert f(L.gqa_prefill_gather(fake, fake, fake, 8, 1, 128, fake, fake, 65, fake, 64,
+                                  None)) == "GQA_ERR_RANGE"
+    assert f(L.gqa_kv_append_chunk(fake, 1, fake, fake, 0, 1, 128, None)) == "GQA_ERR_INVALID_ARG"
+    assert f(L.gqa_kv_append_chunk(fake + 4, 1, fake, fake, 4, 1, 128, None)) == "GQA_ERR_ALIGNMENT"
