@@ -465,6 +465,109 @@ def e2e_decode(w, st, steps, warmup, stream, kv_bytes):
 
 
 # ----------------------------------------------------------------------------------------
+# whole-model decode step (every layer of the hybrid decoder, CUDA graph)
+# ----------------------------------------------------------------------------------------
+
+def bench_decode_model(w, steps, warmup, stream, peaks, peak_src):
+    """One step = kv_append + decode for every layer (7 local ring layers then 1 global
+    linear layer per period), captured once in a CUDA graph and replayed.  Caches and
+    inputs are drawn on the device (synthetic N(0,1), seeded); the descriptor counts are
+    restored at the start of every replay so each step appends into the same slots.
+    Reported against the pages' byte model: K and V read once per (sequence, KV head),
+    4 Hkv d [n_global N + n_local min(N, W)] bytes per sequence."""
+    import numpy as np
+    import torch
+    import global_causal_gqa_gb300 as gqa
+    from global_causal_gqa_gb300 import accounting as acc
+    gen = torch.Generator(device="cuda").manual_seed(w.seed)
+    rnd = lambda *shape: torch.randn(*shape, generator=gen, device="cuda").to(torch.bfloat16)  # noqa: E731
+    tables = {}
+    for is_g, rope, n in ((True, w.rope_global, w.N), (False, w.rope_local, w.W)):
+        f = gqa.gqa_rope_inv_freq(w.d, rope.base, rope.yarn_factor, rope.yarn_L0, rope.beta_fast,
+                                  rope.beta_slow, rope.rotate_fraction)
+        t = torch.empty(n * w.d, dtype=torch.float32, device="cuda")
+        gqa.gqa_rope_table_build(t, f, w.d, rope.amp, n)
+        tables[is_g] = (t, n)
+    layers = []
+    for l in range(w.layers):
+        is_g = (l % w.period) == w.period - 1
+        cap = w.N if is_g else w.W
+        kc = rnd(w.nseq, w.Hkv, cap, w.d)
+        vc = rnd(w.nseq, w.Hkv, cap, w.d)
+        tab, tlen = tables[is_g]
+        a = gqa.make_kv_descs([kc[i] for i in range(w.nseq)], [vc[i] for i in range(w.nseq)],
+                              [tab] * w.nseq, [cap] * w.nseq, [w.N - 1] * w.nseq,
+                              [0 if is_g else 1] * w.nseq, [tlen] * w.nseq)
+        d0 = torch.from_numpy(a.view(np.uint8).copy()).cuda()
+        layers.append({"kc": kc, "vc": vc, "descs0": d0, "descs": d0.clone(),
+                       "q": rnd(w.nseq, w.Hq, w.d), "k_new": rnd(w.nseq, w.Hkv, w.d),
+                       "v_new": rnd(w.nseq, w.Hkv, w.d), "o": torch.empty(w.nseq, w.Hq, w.d,
+                                                                          dtype=torch.bfloat16,
+                                                                          device="cuda")})
+    max_len = w.N
+    wsb = gqa.gqa_decode_workspace_bytes(w.nseq, w.Hq, w.d, max_len)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    n_g = w.layers // w.period
+    n_l = w.layers - n_g
+    bytes_step = w.nseq * 2 * 2 * w.Hkv * w.d * (n_g * w.N + n_l * min(w.N, w.W))
+    assert bytes_step == w.nseq * acc.kv_bytes_per_token(w.layers, w.Hkv, w.d, w.N, w.W)
+
+    def body():
+        for L in layers:
+            L["descs"].copy_(L["descs0"], non_blocking=True)
+            gqa.gqa_kv_append(L["descs"], w.nseq, L["k_new"], L["v_new"], w.Hkv, w.d, None)
+            gqa.gqa_attn_decode(L["q"], L["descs"], w.nseq, w.Hq, w.Hkv, w.d, w.scale, max_len,
+                                L["o"], None, ws, wsb)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def timed(run, n):
+        out = []
+        for _ in range(n):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            out.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in out)
+
+    for _ in range(warmup):
+        body()
+    torch.cuda.synchronize()
+    assert gqa.gqa_get_device_status() == 0
+    eager_ms = timed(body, steps)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            body()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    graph_ms = timed(graph.replay, steps)
+    assert gqa.gqa_get_device_status() == 0
+    peak = peaks["hbm_gbs"]
+    predicted_ms = bytes_step / (peak * 1e9) * 1e3
+    return {
+        "value": bytes_step / (graph_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": graph_ms,
+        "eager_ms_per_step": eager_ms, "kv_bytes_per_step": bytes_step,
+        "byte_model": {"bytes_per_token": bytes_step // w.nseq,
+                       "predicted_ms_at_peak": predicted_ms,
+                       "measured_over_predicted": graph_ms / predicted_ms},
+        "roofline": {"bound": "hbm", "kernel": "64 x (kv_append_kernel + decode_partial_kernel "
+                     "+ decode_combine_kernel), one CUDA graph",
+                     "achieved": bytes_step / (graph_ms * 1e-3) / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": (bytes_step / (graph_ms * 1e-3) / 1e9) / peak,
+                     "peak_source": f"hbm_gbs ({peak_src})", "traffic": None},
+        "gpu_launches": 3 * w.layers * steps,
+    }
+
+
+# ----------------------------------------------------------------------------------------
 # CPU oracle (cpu_baseline leg and --impl reference)
 # ----------------------------------------------------------------------------------------
 
@@ -618,8 +721,10 @@ def main():
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
-    from workloads import DecodeWorkload, get_workload
+    from workloads import DecodeModelWorkload, DecodeWorkload, get_workload
     wl = get_workload(args.workload)
+    if isinstance(wl, DecodeModelWorkload):
+        raise SystemExit(f"{wl.name} is reported in the extras of the default run only")
     if args.layer is not None:
         import dataclasses
         wl = dataclasses.replace(wl, name=f"{wl.name}[layer {args.layer}]",
@@ -650,12 +755,15 @@ def main():
     extra = []
     if world == 1 and not args.no_extra:
         for name in ("plamo3_local_prefill", "plamo3_global_prefill", "plamo3_decode_batch32",
-                     "gemma4_period_6layer", "gemma4_decode_global", "gemma4_decode_local"):
+                     "gemma4_period_6layer", "gemma4_decode_global", "gemma4_decode_local",
+                     "plamo3_decode_64layer"):
             if name == wl.name:
                 continue
             other = get_workload(name)
             ks, kw = min(args.steps, 10), 3
-            if isinstance(other, DecodeWorkload):
+            if isinstance(other, DecodeModelWorkload):
+                r = bench_decode_model(other, ks, kw, stream, peaks, peak_src)
+            elif isinstance(other, DecodeWorkload):
                 r = bench_decode(other, ks, kw, stream, peaks, peak_src, 1, False)
             else:
                 r = bench_prefill(name, list(other.layers), ks, kw, stream, peaks, peak_src, 1,

@@ -21,6 +21,7 @@ from .configs import (  # noqa: F401
     PrefillLayer,
     PrefillWorkload,
     DecodeWorkload,
+    DecodeModelWorkload,
     RopeSpec,
     WORKLOADS,
     get_workload,

@@ -126,9 +126,36 @@ GEMMA4_DECODE_LOCAL = DecodeWorkload(
     global_len_range=(1024, 1024), window=1024, rope_global=_G4_GLOBAL,
     rope_local=_G4_LOCAL, scale=1 / math.sqrt(256), seed=7007)
 
+@dataclass(frozen=True)
+class DecodeModelWorkload:
+    """One decode step through a whole hybrid decoder's attention: `layers` layers in
+    periods of `period` (the last layer of each period global with a linear cache of N
+    tokens, the others local with a ring of W), `nseq` sequences at context N."""
+    name: str
+    layers: int
+    period: int
+    nseq: int
+    N: int
+    W: int
+    Hq: int
+    Hkv: int
+    d: int
+    rope_global: RopeSpec
+    rope_local: RopeSpec
+    scale: float
+    seed: int
+
+
+# PLaMo 3 31B: 64 layers, 7 sliding-window layers then 1 global in each period of 8, at the
+# context N = 4096 of the pages' byte-count table (576 MiB of K/V reads per token).
+PLAMO3_DECODE_64LAYER = DecodeModelWorkload(
+    "plamo3_decode_64layer", layers=64, period=8, nseq=32, N=4096, W=2048, Hq=64, Hkv=8,
+    d=_PLAMO_D, rope_global=_YARN8, rope_local=_LOCAL, scale=1 / math.sqrt(128), seed=8008)
+
 WORKLOADS = {w.name: w for w in (TINY_W64, TINY_CAUSAL, PLAMO3_LOCAL_PREFILL,
                                  PLAMO3_GLOBAL_PREFILL, PLAMO3_DECODE, GEMMA4_PERIOD,
-                                 GEMMA4_DECODE_GLOBAL, GEMMA4_DECODE_LOCAL)}
+                                 GEMMA4_DECODE_GLOBAL, GEMMA4_DECODE_LOCAL,
+                                 PLAMO3_DECODE_64LAYER)}
 
 
 def get_workload(name: str):
