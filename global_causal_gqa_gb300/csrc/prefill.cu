@@ -13,11 +13,12 @@
 // skipping, §1 and §5.3: local prefill costs O(T W)); the per-element mask is applied on
 // the tiles that straddle the diagonal or the window's lower edge only.
 //
-// The kernel is persistent: one CTA per SM walks a list of items (snake order over
-// rounds, so a CTA that drew long causal rows in one round draws short ones in the
-// next).  The per-item fixed work overlaps the previous item: the next item's Q tiles
-// are loaded into the second of two Q buffers and rotated while the current item runs,
-// and the current item's epilogue overlaps the next item's first score products.
+// The kernel is persistent: the grid has one CTA per item, but the CTAs that get an SM
+// claim the items of CTAs not launched yet (cluster launch control), so each SM keeps one
+// CTA that walks items in launch order (longest rows first) and the load balances itself.
+// The per-item fixed work overlaps the previous item: the next item's Q tiles are loaded
+// into the second of two Q buffers and rotated while the current item runs, and the
+// current item's epilogue overlaps the next item's first score products.
 //
 // Warp roles (12 warps, 3 warpgroups; 3 warps per SM sub-partition cap every thread at
 // 168 registers):
@@ -62,7 +63,7 @@ constexpr int kTileBytes = 2 * kBoxBytes;     // 128 rows x 128 bf16
 constexpr int kSmemQ = 0;                     // 2 buffers x 2 query tiles
 constexpr int kSmemRing = 4 * kTileBytes;
 constexpr int kSmemBar = kSmemRing + kSlots * kTileBytes;
-constexpr int kSmemBytes = kSmemBar + 256 + 1024;  // + barriers + alignment slack
+constexpr int kSmemBytes = kSmemBar + 512 + 1024;  // + barriers + alignment slack
 constexpr int kThreads = 384;
 constexpr int kRotThreads = 64;               // warps 2-3
 constexpr uint32_t kTmemCols = 512;
@@ -81,7 +82,13 @@ constexpr int kStreamMinTiles = 48;
 #endif
 constexpr uint32_t kPolyPairs = GQA_PREFILL_POLY_PAIRS;
 
+constexpr int kItemSlots = 4;                 // responses of the work-claiming ring
+constexpr int kItemReaders = 11;              // MMA thread + 2 RoPE warps + 8 softmax warps
+
 struct Bars {
+    uint4 clc_resp[kItemSlots];                   // cluster-launch-control responses
+    uint64_t clc_full[kItemSlots];                // response for item k landed (slot k & 3)
+    uint64_t item_free[kItemSlots];               // every role has read that response
     uint64_t q_full[2], q_ready[2];               // per Q buffer
     uint64_t epi_done[2];                         // the buffer's O staging has been stored
     uint64_t staged[2];                           // per query tile: O rows written to smem
@@ -92,7 +99,7 @@ struct Bars {
     uint64_t mma_done;
     uint32_t tmem_base;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 struct Params {
     __nv_bfloat16 *o;
@@ -127,12 +134,28 @@ __device__ __forceinline__ Item make_item(const Params &p, int idx) {
     return it;
 }
 
-// Index of this CTA's k-th item, or -1 past the end.  Round r covers items
-// [r G, (r + 1) G) with G = gridDim.x; odd rounds are walked backwards.
-__device__ __forceinline__ int item_index(const Params &p, int k) {
-    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-    const long idx = static_cast<long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
-    return idx < p.n_items ? static_cast<int>(idx) : -1;
+// Work items are claimed dynamically: item 0 of a CTA is its own blockIdx.x (the grid has
+// one CTA per item), and during item k the producer asks the hardware to cancel one CTA
+// that has not been launched yet and takes over its item as item k + 1 (cluster launch
+// control).  CTAs that finish early thus take more items, in launch order (longest rows
+// first), without any counter in memory.  The responses go through a 4-slot ring that
+// every role reads.
+
+// Item j >= 1 of a CTA has its response in slot (j - 1) % 4, the ((j - 1) / 4)-th use of
+// that slot (item 0 is the CTA's own index and has no response).
+__device__ __forceinline__ int item_slot(int j) { return (j - 1) & (kItemSlots - 1); }
+__device__ __forceinline__ int item_use(int j) { return (j - 1) / kItemSlots; }
+
+// Item k (k >= 1) of this CTA for a reader role: waits for the response, decodes it.
+// Returns -1 when nothing was left to claim (or the wait expired: *ok is cleared).
+__device__ __forceinline__ int read_item(Bars *bars, int k, int n_items, bool &ok) {
+    const int slot = item_slot(k);
+    if (!mbar_wait(&bars->clc_full[slot], item_use(k) & 1)) {
+        ok = false;
+        return -1;
+    }
+    const int x = clc_decode(&bars->clc_resp[slot]);
+    return x < n_items ? x : -1;
 }
 
 // A bounded wait whose outcome every lane of the warp agrees on, so the warp-collective
@@ -173,6 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
+        for (int i = 0; i < kItemSlots; ++i) {
+            mbar_init(&bars->clc_full[i], 1);
+            mbar_init(&bars->item_free[i], kItemReaders);
+        }
         mbar_init(&bars->mma_done, 1);
         fence_mbar_init();
     }
@@ -195,8 +222,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int u = 0;          // ring loads issued
             int q_issued = 0;   // items whose Q tiles have been issued
-            auto load_q = [&](int k) {
-                const Item it = make_item(p, item_index(p, k));
+            // claims item k (k >= 1) of this CTA: one cancellation request into its slot, once
+            // every role has read the slot's previous response (item k - 4)
+            auto claim = [&](int k) {
+                const int slot = item_slot(k);
+                if (k > kItemSlots &&
+                    !(ok = mbar_wait(&bars->item_free[slot], (item_use(k) - 1) & 1))) {
+                    set_timeout(p.status, kDiagPrefill, kRoleProducer, 2, k);
+                    return;
+                }
+                mbar_arrive_expect_tx(&bars->clc_full[slot], 16);
+                clc_try_cancel(&bars->clc_resp[slot], &bars->clc_full[slot]);
+            };
+            auto load_q = [&](int k, int idx) {
+                const Item it = make_item(p, idx);
                 const int buf = k & 1;
                 // buffer reuse: item k - 2 is finished and its O, staged in this buffer,
                 // has been read out by the TMA stores
@@ -225,10 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(dst + kBoxBytes, map, &bars->full[st], 64, n0, zk);
                 ++u;
             };
-            if (item_index(p, 0) >= 0) load_q(0);
-            for (int k = 0; ok && item_index(p, k) >= 0; ++k) {
-                const Item it = make_item(p, item_index(p, k));
-                const bool has_next = item_index(p, k + 1) >= 0;
+            int idx = blockIdx.x;
+            load_q(0, idx);
+            for (int k = 0; ok && idx >= 0; ++k) {
+                const Item it = make_item(p, idx);
+                claim(k + 1);   // one item ahead: its Q is loaded during this one
+                int next = -1;
                 const int zk = it.b * p.Hkv + it.g;
                 // K(0), V(0), K(1), V(1), ...; the next item's Q after the fourth load, by
                 // which time the MMA thread has moved on to this item
@@ -237,8 +278,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int l = 0; l < n_loads && ok; ++l) {
                     const int n0 = (it.kt_first + (l >> 1)) * kBN;
                     put((l & 1) ? &tmV : &tmK, n0, zk);
-                    if (l == q_at && has_next && ok) load_q(k + 1);
+                    if (l == q_at && ok) {
+                        next = read_item(bars, k + 1, p.n_items, ok);
+                        if (!ok) set_timeout(p.status, kDiagPrefill, kRoleProducer, 3, k + 1);
+                        if (next >= 0) load_q(k + 1, next);
+                    }
                 }
+                idx = next;
             }
             if (!ok) {
                 // never leave the CTA with copies in flight
@@ -295,8 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     set_timeout(p.status, kDiagPrefill, kRoleMma, where, cpv[i]);
                 tc_fence_after();
             };
-            for (int k = 0; ok && item_index(p, k) >= 0; ++k) {
-                const Item it = make_item(p, item_index(p, k));
+            for (int k = 0, idx = blockIdx.x; ok && idx >= 0; ++k) {
+                const Item it = make_item(p, idx);
                 const int buf = k & 1, ntile = it.two ? 2 : 1, n = it.n_tiles;
                 const uint32_t qaddr[2] = {smem_u32(sQ(buf, 0)), smem_u32(sQ(buf, 1))};
                 if (!(ok = mbar_wait(&bars->q_ready[buf], (k >> 1) & 1))) {
@@ -344,6 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 for (int i = 0; i < ntile; ++i) ++nepi[i];
+                idx = read_item(bars, k + 1, p.n_items, ok);
+                if (!ok) {
+                    set_timeout(p.status, kDiagPrefill, kRoleMma, 6, k + 1);
+                    break;
+                }
+                mbar_arrive(&bars->item_free[item_slot(k + 1)]);
             }
             if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
             // every tcgen05 operation issued above completes before TMEM is released
@@ -356,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7); the pair
         // (j, j + 64) is the same offset in box 0 and box 1
         const int rt = threadIdx.x - 64;   // 0..63
-        for (int k = 0; item_index(p, k) >= 0; ++k) {
-            const Item it = make_item(p, item_index(p, k));
+        for (int k = 0, idx = blockIdx.x; idx >= 0; ++k) {
+            const Item it = make_item(p, idx);
             const int buf = k & 1;
             if (!warp_wait(&bars->q_full[buf], (k >> 1) & 1)) {
                 set_timeout(p.status, kDiagPrefill, kRoleRope, 0, k);
@@ -405,6 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars->q_ready[buf]);
+            bool ok = true;
+            idx = __shfl_sync(0xffffffffu, read_item(bars, k + 1, p.n_items, ok), 0);
+            if (!__all_sync(0xffffffffu, ok)) {
+                set_timeout(p.status, kDiagPrefill, kRoleRope, 1, k + 1);
+                break;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->item_free[item_slot(k + 1)]);
         }
     } else {
         // ================= softmax / epilogue =================
@@ -417,11 +477,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         int pvb = 0;   // PV products of the previous items
         int ne = 0;    // items finished
         bool ok = true;
-        for (int k = 0; ok && item_index(p, k) >= 0; ++k) {
+        for (int k = 0, idx = blockIdx.x; ok && idx >= 0; ++k) {
+            // the item after this one (read at the end of the loop body)
+            auto advance = [&]() {
+                bool rok = true;
+                const int nx = __shfl_sync(0xffffffffu, read_item(bars, k + 1, p.n_items, rok), 0);
+                if (!__all_sync(0xffffffffu, rok)) {
+                    set_timeout(p.status, kDiagPrefill, kRoleSoftmax, 4, k + 1);
+                    ok = false;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->item_free[item_slot(k + 1)]);
+                idx = nx;
+            };
             int n_tiles, kt_first, qpos;
             {
-                const Item it = make_item(p, item_index(p, k));
-                if (wg == 1 && !it.two) continue;
+                const Item it = make_item(p, idx);
+                if (wg == 1 && !it.two) {
+                    advance();
+                    continue;
+                }
                 n_tiles = it.n_tiles;
                 kt_first = it.kt_first;
                 qpos = p.S - p.T + it.mb * kBM + r;
@@ -572,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars->staged[wg]);
-            const Item it = make_item(p, item_index(p, k));
+            const Item it = make_item(p, idx);
             if (r == 0) {
                 if (!mbar_wait(&bars->staged[wg], ne & 1)) {
                     set_timeout(p.status, kDiagPrefill, kRoleSoftmax, 3, ne);
@@ -594,6 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.lse[((size_t)it.b * p.Hq + it.h0 + wg) * p.T + t] =
                     (m + __log2f(l)) * 0.69314718055994531f;
             }
+            advance();
         }
         // the O stores complete before the CTA exits
         if (r == 0) bulk_wait_all();
@@ -667,13 +743,10 @@ int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, flo
         !make_map(&mv, v, d, S, B * Hkv) || !make_map(&mo, o, d, T, B * Hq))
         return GQA_ERR_CUDA;
     static bool attr_done = false;
-    static int sm_count = 0;
     if (!attr_done) {
-        int dev = 0;
-        if (cudaFuncSetAttribute(prefill_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess ||
-            cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        if (cudaFuncSetAttribute(prefill_persistent_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess)
             return GQA_ERR_CUDA;   // the error stays readable with cudaGetLastError
         attr_done = true;
     }
@@ -694,8 +767,9 @@ int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, flo
     const long n_items = (long)B * Hkv * p.n_pairs * p.n_mblocks;
     if (n_items > 0x7fffffffL) return GQA_ERR_UNSUPPORTED;
     p.n_items = static_cast<int>(n_items);
-    const int grid = static_cast<int>(n_items < sm_count ? n_items : sm_count);
-    prefill_persistent_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, p);
+    // one CTA per item; the CTAs that get an SM first claim the rest (cluster launch control)
+    prefill_persistent_kernel<<<static_cast<unsigned>(n_items), kThreads, kSmemBytes, s>>>(
+        mq, mk, mv, mo, p);
     const cudaError_t e = cudaPeekAtLastError();
     return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }

@@ -140,6 +140,33 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// ---- cluster launch control (dynamic work for persistent CTAs) ------------------------
+// Asks the hardware to cancel one CTA of this grid that has not been launched yet; the
+// 16-byte response is written to `resp` and completes 16 bytes of transaction on `bar`
+// (arm it with mbar_arrive_expect_tx(bar, 16) first).  Never issue another request after
+// a response that reported no cancellation.
+__device__ __forceinline__ void clc_try_cancel(void *resp, uint64_t *bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+        "[%0], [%1];" ::"r"(smem_u32(resp)),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+// The x index of the cancelled CTA in a response, or -1 if nothing was cancelled.
+__device__ __forceinline__ int clc_decode(const void *resp) {
+    uint32_t canceled, x = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(canceled), "+r"(x)
+        : "r"(smem_u32(resp))
+        : "memory");
+    return canceled ? static_cast<int>(x) : -1;
+}
+
 __device__ __forceinline__ void mbar_arrive_cnt(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                  : "memory");
