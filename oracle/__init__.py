@@ -78,6 +78,12 @@ def _load(plant: int = 0) -> ctypes.CDLL:
         lib.orc_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, D,
                                         P, P, P, P, I]
         lib.orc_decode_step.restype = I
+        lib.orc_attention_kv_shared.argtypes = [P, P, P, P, D, I, I, I, I, I, I, I, D, P, D,
+                                                P, L, P, P, I]
+        lib.orc_attention_kv_shared.restype = I
+        lib.orc_decode_step_kv_shared.argtypes = [P, P, P, P, P, P, P, P, P, P, D, I, I, I, I,
+                                                  D, P, P, P, P, I]
+        lib.orc_decode_step_kv_shared.restype = I
         lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.orc_bf16_to_double.restype = D
         lib.orc_allowed_pub.argtypes = [L, L, I]
@@ -231,6 +237,74 @@ class Oracle:
             _ptr(o), _ptr(lse), _ptr(slots), _ptr(after), int(nthreads))
         if rc != 0:
             raise ValueError(f"orc_decode_step failed ({rc})")
+        return o, lse, slots, after
+
+
+    # -- shared K/V projection (Gemma 4 global layers, [PL3] §5.2 and §8) ----------------
+    @staticmethod
+    def _gain(g):
+        return None if g is None else np.ascontiguousarray(g, dtype=np.float64)
+
+    def attention_kv_shared(self, q, z, *, q_gamma, k_gamma, eps: float, window: int,
+                            scale: float, w: np.ndarray, amp: float,
+                            rows: Optional[np.ndarray] = None, nthreads: int = 0):
+        """attention_k_eq_v: q [B,Hq,T,d] (before its norm) and the shared projection
+        output z [B,Hkv,S,d] (bf16).  Q' = RoPE(N_{q_gamma}(q)), K' = RoPE(N_{k_gamma}(z)),
+        V = N_1(z).  Gains None mean 1.  Returns (o, lse) shaped as attention()."""
+        qb, zb = _bits(q), _bits(z)
+        B, Hq, T, d = qb.shape
+        _, Hkv, S, _ = zb.shape
+        w = np.ascontiguousarray(w, dtype=np.float64)
+        gq, gk = self._gain(q_gamma), self._gain(k_gamma)
+        if rows is not None:
+            rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 3)
+            n = rows.shape[0]
+        else:
+            n = B * Hq * T
+        o = np.zeros((n, d), dtype=np.float64)
+        lse = np.zeros(n, dtype=np.float64)
+        rc = self.lib.orc_attention_kv_shared(
+            _ptr(qb), _ptr(zb), None if gq is None else _ptr(gq),
+            None if gk is None else _ptr(gk), float(eps), B, T, S, Hq, Hkv, d, int(window),
+            float(scale), _ptr(w), float(amp), _ptr(rows) if rows is not None else None,
+            n if rows is not None else 0, _ptr(o), _ptr(lse), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"orc_attention_kv_shared failed ({rc})")
+        if rows is None:
+            o = o.reshape(B, Hq, T, d)
+            lse = lse.reshape(B, Hq, T)
+        return o, lse
+
+    def decode_step_kv_shared(self, q, z_new, z_cache: Sequence, cap: Sequence[int],
+                              count_before: Sequence[int], is_ring: Sequence[int],
+                              w: Sequence[np.ndarray], amp: Sequence[float], *, q_gamma,
+                              k_gamma, eps: float, scale: float, nthreads: int = 0):
+        """One decode step of a shared-projection layer over caches of projection outputs
+        Z.  Returns (o [nseq,Hq,d], lse [nseq,Hq], slots, counts)."""
+        qb, znb = _bits(q), _bits(z_new)
+        nseq, Hq, d = qb.shape
+        Hkv = znb.shape[1]
+        zc = [_bits(t) for t in z_cache]
+        zp = (ctypes.c_void_p * nseq)(*[c.ctypes.data for c in zc])
+        ws = [np.ascontiguousarray(x, dtype=np.float64) for x in w]
+        wp = (ctypes.c_void_p * nseq)(*[x.ctypes.data for x in ws])
+        capa = np.asarray(cap, dtype=np.int64)
+        cnt = np.asarray(count_before, dtype=np.int64)
+        ring = np.asarray(is_ring, dtype=np.int32)
+        ampa = np.asarray(amp, dtype=np.float64)
+        gq, gk = self._gain(q_gamma), self._gain(k_gamma)
+        o = np.zeros((nseq, Hq, d), dtype=np.float64)
+        lse = np.zeros((nseq, Hq), dtype=np.float64)
+        slots = np.zeros(nseq, dtype=np.int64)
+        after = np.zeros(nseq, dtype=np.int64)
+        rc = self.lib.orc_decode_step_kv_shared(
+            _ptr(qb), _ptr(znb), ctypes.cast(zp, ctypes.c_void_p), _ptr(capa), _ptr(cnt),
+            _ptr(ring), ctypes.cast(wp, ctypes.c_void_p), _ptr(ampa),
+            None if gq is None else _ptr(gq), None if gk is None else _ptr(gk), float(eps),
+            nseq, Hq, Hkv, d, float(scale), _ptr(o), _ptr(lse), _ptr(slots), _ptr(after),
+            int(nthreads))
+        if rc != 0:
+            raise ValueError(f"orc_decode_step_kv_shared failed ({rc})")
         return o, lse, slots, after
 
 

@@ -28,6 +28,9 @@
  *               the exponent's denominator stays the full head dimension;
  *         §3.2, §4.3  RMSNorm with an effective gain (offset + weight), per head for
  *               q_norm / k_norm (offset 1, eps 1e-6); V is not normalised.
+ *         §5.2, §8  Gemma 4's global layers share one projection for K and V
+ *               (attention_k_eq_v): with Z its output, K = RoPE(N_{gamma_k}(Z)) and
+ *               V = N_1(Z), the gain-free RMSNorm.
  *   [LLA] disassemble-channel.com LLaMA tutorial, GQA section: g(i) = floor(i n_kv / h),
  *         the same grouping written with the KV-head count.
  *
@@ -178,19 +181,85 @@ static int orc_kv_head(int h, int Hq, int Hkv) {
 
 int orc_kv_head_pub(int h, int Hq, int Hkv) { return orc_kv_head(h, Hq, Hkv); }
 
-/* Attention rows, fp64.
- *   q : [B, Hq, T, d] bf16 bits     k, v : [B, Hkv, S, d] bf16 bits (k before RoPE)
- *   Query t has position S - T + t, key s has position s ([PL3 §4.4]); pos_shift is
- *   added to every position before the rotation (the mask uses the differences only).
- *   rows : nrows triples (b, h, t), or NULL for all B*Hq*T rows in (b, h, t) order.
- *   o    : [nrows, d] outputs; lse: [nrows] natural-log sum of exp of the scaled
- *          scores (nullable); weights: [nrows, S] attention weights (nullable).
- * Returns 0, or -1 on a bad argument, -2 on allocation failure. */
-int orc_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                  int B, int T, int S, int Hq, int Hkv, int d, int window, double scale,
-                  const double *w, double amp, long pos_shift,
-                  const int32_t *rows, long nrows,
-                  double *o, double *lse, double *weights, int nthreads) {
+/* [PL3 §4.5, §5.1] one query row: scores of the rotated query qr against the rotated
+ * keys Kr [S, d], the mask, the softmax over the visible keys and the weighted sum of
+ * V [S, d].  z [S] and ok [S] are scratch; lse and wrow (the weights, [S]) are nullable. */
+static void orc_attend_row(const double *qr, const double *Kr, const double *Vd, long S,
+                           int d, long qpos, int window, double scale, double *z, char *ok,
+                           double *orow, double *lse, double *wrow) {
+    double m = -INFINITY;
+    for (long s = 0; s < S; ++s) {
+        ok[s] = (char)orc_allowed(qpos, s, window);
+        if (!ok[s]) { z[s] = -INFINITY; continue; }
+        const double *kr = Kr + (size_t)s * d;
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c) acc += qr[c] * kr[c];
+#if ORC_PLANT == 4
+        z[s] = acc;                   /* planted: scale dropped */
+#else
+        z[s] = acc * scale;
+#endif
+        if (z[s] > m) m = z[s];
+    }
+    double l = 0.0;
+    for (long s = 0; s < S; ++s) l += ok[s] ? exp(z[s] - m) : 0.0;
+    for (int c = 0; c < d; ++c) orow[c] = 0.0;
+    for (long s = 0; s < S; ++s) {
+        if (!ok[s]) continue;
+        const double a = exp(z[s] - m) / l;
+        const double *vr = Vd + (size_t)s * d;
+        for (int c = 0; c < d; ++c) orow[c] += a * vr[c];
+    }
+    if (lse) *lse = m + log(l);
+    if (wrow)
+        for (long s = 0; s < S; ++s) wrow[s] = ok[s] ? exp(z[s] - m) / l : 0.0;
+}
+
+/* The (b, h, t) of requested row r: from the rows array, or row-major (b, h, t) order. */
+static void orc_row_coords(const int32_t *rows, long r, int Hq, int T, int *b, int *h, int *t) {
+    if (rows) { *b = rows[3 * r]; *h = rows[3 * r + 1]; *t = rows[3 * r + 2]; }
+    else { *b = (int)(r / ((long)Hq * T)); *h = (int)((r / T) % Hq); *t = (int)(r % T); }
+}
+
+/* How a layer turns its stored inputs into Q, K' and V (fp64), one vector at a time.
+ *   plain  : Q, K, V as given (bf16 bits), K and Q then rotated ([PL3 §4.4]);
+ *   shared : Gemma 4's global layers (attention_k_eq_v, [PL3 §8] and [PL3 §5.2]): one
+ *            projection output Z per KV head gives both K = RoPE(N_{gamma_k}(Z)) and
+ *            V = N_1(Z) (RMSNorm without a gain); the query is N_{gamma_q}(q), rotated. */
+typedef struct {
+    int shared;
+    const double *q_gamma, *k_gamma;   /* shared only (NULL = gain 1) */
+    double eps;
+} orc_inputs;
+
+static void orc_load_q(const orc_inputs *in, const uint16_t *src, int d, double *out) {
+    if (in->shared) orc_rms_norm(src, 1, d, in->q_gamma, in->eps, out);
+    else for (int c = 0; c < d; ++c) out[c] = bf16_to_f64(src[c]);
+}
+
+/* key s: kr = K (not yet rotated), vr = V, from the stored rows ks and vs */
+static void orc_load_kv(const orc_inputs *in, const uint16_t *ks, const uint16_t *vs, int d,
+                        double *kr, double *vr) {
+    if (in->shared) {
+        orc_rms_norm(ks, 1, d, in->k_gamma, in->eps, kr);
+#if ORC_PLANT == 9
+        orc_rms_norm(ks, 1, d, in->k_gamma, in->eps, vr);   /* planted: V keeps K's gain */
+#else
+        orc_rms_norm(ks, 1, d, NULL, in->eps, vr);
+#endif
+    } else {
+        for (int r = 0; r < d; ++r) {
+            kr[r] = bf16_to_f64(ks[r]);
+            vr[r] = bf16_to_f64(vs[r]);
+        }
+    }
+}
+
+static int orc_attention_impl(const orc_inputs *in, const uint16_t *q, const uint16_t *k,
+                              const uint16_t *v, int B, int T, int S, int Hq, int Hkv, int d,
+                              int window, double scale, const double *w, double amp,
+                              long pos_shift, const int32_t *rows, long nrows, double *o,
+                              double *lse, double *weights, int nthreads) {
     if (!q || !k || !v || !w || !o || B <= 0 || T <= 0 || S <= 0 || T > S || Hq <= 0 ||
         Hkv <= 0 || (Hq % Hkv) != 0 || d <= 0 || (d % 2) != 0)
         return -1;
@@ -211,22 +280,19 @@ int orc_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             /* the requested rows whose query head reads KV head g of batch b */
             long nsel = 0;
             for (long r = 0; r < total; ++r) {
-                int rb, rh;
-                if (rows) { rb = rows[3 * r]; rh = rows[3 * r + 1]; }
-                else { rb = (int)(r / ((long)Hq * T)); rh = (int)((r / T) % Hq); }
+                int rb, rh, rt;
+                orc_row_coords(rows, r, Hq, T, &rb, &rh, &rt);
                 if (rb == b && orc_kv_head(rh, Hq, Hkv) == g) sel[nsel++] = r;
             }
             if (nsel == 0) continue;
             const uint16_t *kb = k + ((size_t)b * Hkv + g) * (size_t)S * d;
             const uint16_t *vb = v + ((size_t)b * Hkv + g) * (size_t)S * d;
-            /* K' = RoPE(K) at positions 0..S-1 ([PL3 §4.4]); V as stored. */
+            /* K' = RoPE(K) at positions 0..S-1 ([PL3 §4.4]); V as the layer defines it. */
 #pragma omp parallel for schedule(static)
             for (long s = 0; s < S; ++s) {
                 double *kr = Kr + (size_t)s * d;
-                for (int r = 0; r < d; ++r) {
-                    kr[r] = bf16_to_f64(kb[(size_t)s * d + r]);
-                    Vd[(size_t)s * d + r] = bf16_to_f64(vb[(size_t)s * d + r]);
-                }
+                orc_load_kv(in, kb + (size_t)s * d, vb + (size_t)s * d, d, kr,
+                            Vd + (size_t)s * d);
                 orc_rope_rotate(kr, d, (double)(s + pos_shift), w, amp);
             }
 #pragma omp parallel
@@ -238,44 +304,14 @@ int orc_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 for (long i = 0; i < nsel; ++i) {
                     if (!qr || !z || !ok) continue;
                     const long r = sel[i];
-                    int rh, rt;
-                    if (rows) { rh = rows[3 * r + 1]; rt = rows[3 * r + 2]; }
-                    else { rh = (int)((r / T) % Hq); rt = (int)(r % T); }
+                    int rb, rh, rt;
+                    orc_row_coords(rows, r, Hq, T, &rb, &rh, &rt);
                     const long qpos = (long)(S - T) + rt;
-                    const uint16_t *qb = q + (((size_t)b * Hq + rh) * T + rt) * (size_t)d;
-                    for (int c = 0; c < d; ++c) qr[c] = bf16_to_f64(qb[c]);
+                    orc_load_q(in, q + (((size_t)b * Hq + rh) * T + rt) * (size_t)d, d, qr);
                     orc_rope_rotate(qr, d, (double)(qpos + pos_shift), w, amp);
-                    /* scores and mask ([PL3 §4.5, §5.1]) */
-                    double m = -INFINITY;
-                    for (long s = 0; s < S; ++s) {
-                        ok[s] = (char)orc_allowed(qpos, s, window);
-                        if (!ok[s]) { z[s] = -INFINITY; continue; }
-                        const double *kr = Kr + (size_t)s * d;
-                        double acc = 0.0;
-                        for (int c = 0; c < d; ++c) acc += qr[c] * kr[c];
-#if ORC_PLANT == 4
-                        z[s] = acc;                   /* planted: scale dropped */
-#else
-                        z[s] = acc * scale;
-#endif
-                        if (z[s] > m) m = z[s];
-                    }
-                    /* softmax over the visible keys, then the weighted sum of V */
-                    double l = 0.0;
-                    for (long s = 0; s < S; ++s) l += ok[s] ? exp(z[s] - m) : 0.0;
-                    double *orow = o + (size_t)r * d;
-                    for (int c = 0; c < d; ++c) orow[c] = 0.0;
-                    for (long s = 0; s < S; ++s) {
-                        if (!ok[s]) continue;
-                        const double a = exp(z[s] - m) / l;
-                        const double *vr = Vd + (size_t)s * d;
-                        for (int c = 0; c < d; ++c) orow[c] += a * vr[c];
-                    }
-                    if (lse) lse[r] = m + log(l);
-                    if (weights) {
-                        double *wr = weights + (size_t)r * S;
-                        for (long s = 0; s < S; ++s) wr[s] = ok[s] ? exp(z[s] - m) / l : 0.0;
-                    }
+                    orc_attend_row(qr, Kr, Vd, S, d, qpos, window, scale, z, ok,
+                                   o + (size_t)r * d, lse ? lse + r : NULL,
+                                   weights ? weights + (size_t)r * S : NULL);
                 }
                 free(qr); free(z); free(ok);
             }
@@ -283,6 +319,41 @@ int orc_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     }
     free(Kr); free(Vd); free(sel);
     return 0;
+}
+
+/* Attention rows, fp64.
+ *   q : [B, Hq, T, d] bf16 bits     k, v : [B, Hkv, S, d] bf16 bits (k before RoPE)
+ *   Query t has position S - T + t, key s has position s ([PL3 §4.4]); pos_shift is
+ *   added to every position before the rotation (the mask uses the differences only).
+ *   rows : nrows triples (b, h, t), or NULL for all B*Hq*T rows in (b, h, t) order.
+ *   o    : [nrows, d] outputs; lse: [nrows] natural-log sum of exp of the scaled
+ *          scores (nullable); weights: [nrows, S] attention weights (nullable).
+ * Returns 0, or -1 on a bad argument, -2 on allocation failure. */
+int orc_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  int B, int T, int S, int Hq, int Hkv, int d, int window, double scale,
+                  const double *w, double amp, long pos_shift,
+                  const int32_t *rows, long nrows,
+                  double *o, double *lse, double *weights, int nthreads) {
+    const orc_inputs in = {0, NULL, NULL, 0.0};
+    return orc_attention_impl(&in, q, k, v, B, T, S, Hq, Hkv, d, window, scale, w, amp,
+                              pos_shift, rows, nrows, o, lse, weights, nthreads);
+}
+
+/* Attention of a layer whose K and V share one projection (Gemma 4 global layers,
+ * attention_k_eq_v, [PL3 §5.2 and §8]), fp64:
+ *   q : [B, Hq, T, d] bf16 bits, the query projection before its norm;
+ *   z : [B, Hkv, S, d] bf16 bits, the shared projection output Z;
+ *   Q' = RoPE(N_{q_gamma}(q)), K' = RoPE(N_{k_gamma}(Z)), V = N_1(Z) with
+ *   N_gamma(x) = gamma (*) x / sqrt(mean(x^2) + eps) ([PL3 §3.2]; NULL gamma = gain 1).
+ * Positions, mask, rows and outputs as orc_attention (pos_shift 0). */
+int orc_attention_kv_shared(const uint16_t *q, const uint16_t *z, const double *q_gamma,
+                            const double *k_gamma, double eps, int B, int T, int S, int Hq,
+                            int Hkv, int d, int window, double scale, const double *w,
+                            double amp, const int32_t *rows, long nrows, double *o,
+                            double *lse, int nthreads) {
+    const orc_inputs in = {1, q_gamma, k_gamma, eps};
+    return orc_attention_impl(&in, q, z, z, B, T, S, Hq, Hkv, d, window, scale, w, amp, 0,
+                              rows, nrows, o, lse, NULL, nthreads);
 }
 
 /* ---- cache index model ([PL3 §4.4]) ----------------------------------------------
@@ -314,6 +385,61 @@ long orc_logical_slot(int is_ring, long count_after, long cap, long t) {
 #endif
 }
 
+/* Gathers the R logical keys of sequence i after the append, in age order, from its
+ * cache rows and the new row (placed where its slot appears): out [Hkv, R, d]. */
+static void orc_gather_logical(const uint16_t *cache, const uint16_t *new_row, long cap,
+                               int is_ring, long slot, long after, long R, int Hkv, int d,
+                               uint16_t *out) {
+    for (int g = 0; g < Hkv; ++g) {
+        for (long t = 0; t < R; ++t) {
+            const long sl = orc_logical_slot(is_ring, after, cap, t);
+            const uint16_t *src = (sl == slot) ? new_row + (size_t)g * d
+                                               : cache + ((size_t)g * cap + sl) * d;
+            memcpy(out + ((size_t)g * R + t) * d, src, sizeof(uint16_t) * d);
+        }
+    }
+}
+
+static int orc_decode_impl(const orc_inputs *in, const uint16_t *q, const uint16_t *k_new,
+                           const uint16_t *v_new, const uint16_t *const *k_cache,
+                           const uint16_t *const *v_cache, const int64_t *cap,
+                           const int64_t *count_before, const int32_t *is_ring,
+                           const double *const *w, const double *amp, int nseq, int Hq,
+                           int Hkv, int d, double scale, double *o, double *lse,
+                           int64_t *slot_out, int64_t *count_out, int nthreads) {
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !cap || !count_before ||
+        !is_ring || !w || !amp || !o || nseq <= 0 || Hq <= 0 || Hkv <= 0 ||
+        (Hq % Hkv) != 0 || d <= 0)
+        return -1;
+    for (int i = 0; i < nseq; ++i) {
+        const long c = cap[i];
+        const long slot = orc_append_slot(is_ring[i], count_before[i], c);
+        if (slot < 0) return -1;
+        const long after = count_before[i] + 1;
+        const long R = orc_retained(is_ring[i], after, c);
+        uint16_t *kg = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)Hkv * R * d);
+        uint16_t *vg = in->shared ? kg
+                                  : (uint16_t *)malloc(sizeof(uint16_t) * (size_t)Hkv * R * d);
+        if (!kg || !vg) { free(kg); if (vg != kg) free(vg); return -2; }
+        orc_gather_logical(k_cache[i], k_new + (size_t)i * Hkv * d, c, is_ring[i], slot,
+                           after, R, Hkv, d, kg);
+        if (!in->shared)
+            orc_gather_logical(v_cache[i], v_new + (size_t)i * Hkv * d, c, is_ring[i], slot,
+                               after, R, Hkv, d, vg);
+        const int window = is_ring[i] ? (int)c : 0;
+        int rc = orc_attention_impl(in, q + (size_t)i * Hq * d, kg, vg, 1, 1, (int)R, Hq, Hkv,
+                                    d, window, scale, w[i], amp[i], 0, NULL, 0,
+                                    o + (size_t)i * Hq * d, lse ? lse + (size_t)i * Hq : NULL,
+                                    NULL, nthreads);
+        if (vg != kg) free(vg);
+        free(kg);
+        if (rc != 0) return rc;
+        if (slot_out) slot_out[i] = slot;
+        if (count_out) count_out[i] = after;
+    }
+    return 0;
+}
+
 /* One decode step over a batch: append each sequence's new K/V, then attend with its
  * one query over the logical keys.  Caches are read, never written: the appended token
  * is taken from k_new/v_new where its slot appears.
@@ -329,43 +455,27 @@ int orc_decode_step(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_
                     int nseq, int Hq, int Hkv, int d, double scale,
                     double *o, double *lse, int64_t *slot_out, int64_t *count_out,
                     int nthreads) {
-    if (!q || !k_new || !v_new || !k_cache || !v_cache || !cap || !count_before ||
-        !is_ring || !w || !amp || !o || nseq <= 0 || Hq <= 0 || Hkv <= 0 ||
-        (Hq % Hkv) != 0 || d <= 0)
-        return -1;
-    for (int i = 0; i < nseq; ++i) {
-        const long c = cap[i];
-        const long slot = orc_append_slot(is_ring[i], count_before[i], c);
-        if (slot < 0) return -1;
-        const long after = count_before[i] + 1;
-        const long R = orc_retained(is_ring[i], after, c);
-        uint16_t *kg = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)Hkv * R * d);
-        uint16_t *vg = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)Hkv * R * d);
-        if (!kg || !vg) { free(kg); free(vg); return -2; }
-        for (int g = 0; g < Hkv; ++g) {
-            for (long t = 0; t < R; ++t) {
-                const long sl = orc_logical_slot(is_ring[i], after, c, t);
-                const uint16_t *ks, *vs;
-                if (sl == slot) {
-                    ks = k_new + ((size_t)i * Hkv + g) * d;
-                    vs = v_new + ((size_t)i * Hkv + g) * d;
-                } else {
-                    ks = k_cache[i] + ((size_t)g * c + sl) * d;
-                    vs = v_cache[i] + ((size_t)g * c + sl) * d;
-                }
-                memcpy(kg + ((size_t)g * R + t) * d, ks, sizeof(uint16_t) * d);
-                memcpy(vg + ((size_t)g * R + t) * d, vs, sizeof(uint16_t) * d);
-            }
-        }
-        const int window = is_ring[i] ? (int)c : 0;
-        int rc = orc_attention(q + (size_t)i * Hq * d, kg, vg, 1, 1, (int)R, Hq, Hkv, d,
-                               window, scale, w[i], amp[i], 0, NULL, 0,
-                               o + (size_t)i * Hq * d, lse ? lse + (size_t)i * Hq : NULL,
-                               NULL, nthreads);
-        free(kg); free(vg);
-        if (rc != 0) return rc;
-        if (slot_out) slot_out[i] = slot;
-        if (count_out) count_out[i] = after;
-    }
-    return 0;
+    const orc_inputs in = {0, NULL, NULL, 0.0};
+    return orc_decode_impl(&in, q, k_new, v_new, k_cache, v_cache, cap, count_before, is_ring,
+                           w, amp, nseq, Hq, Hkv, d, scale, o, lse, slot_out, count_out,
+                           nthreads);
+}
+
+/* One decode step of a layer whose K and V share one projection (attention_k_eq_v,
+ * [PL3 §5.2 and §8]): the cache of sequence i holds the projection outputs Z of its past
+ * tokens ([Hkv, cap, d], slots as stored), z_new [nseq, Hkv, d] the new token's, q
+ * [nseq, Hq, d] its query before the norm.  Appends as orc_decode_step, then attends with
+ * Q' = RoPE(N_{q_gamma}(q)), K' = RoPE(N_{k_gamma}(Z)), V = N_1(Z) over the logical keys. */
+int orc_decode_step_kv_shared(const uint16_t *q, const uint16_t *z_new,
+                              const uint16_t *const *z_cache, const int64_t *cap,
+                              const int64_t *count_before, const int32_t *is_ring,
+                              const double *const *w, const double *amp,
+                              const double *q_gamma, const double *k_gamma, double eps,
+                              int nseq, int Hq, int Hkv, int d, double scale, double *o,
+                              double *lse, int64_t *slot_out, int64_t *count_out,
+                              int nthreads) {
+    const orc_inputs in = {1, q_gamma, k_gamma, eps};
+    return orc_decode_impl(&in, q, z_new, z_new, z_cache, z_cache, cap, count_before, is_ring,
+                           w, amp, nseq, Hq, Hkv, d, scale, o, lse, slot_out, count_out,
+                           nthreads);
 }

@@ -385,7 +385,69 @@ def check_rms_norm_scale_invariance(orc):
     assert np.max(np.abs(a - b)) < 1e-5, np.max(np.abs(a - b))
 
 
+# ---------------------------------------------------------------------------------
+# shared K/V projection (attention_k_eq_v of Gemma 4's global layers: PLaMo page §5.2
+# and §8 -- K = RoPE(N_{gamma_k}(Z)), V = N_1(Z))
+# ---------------------------------------------------------------------------------
+
+def _gains(d, seed, level):
+    g = torch.Generator().manual_seed(seed)
+    return level * (1.0 + 0.2 * torch.randn(d, generator=g, dtype=torch.float64)).numpy()
+
+
+def check_kv_shared_library(orc):
+    """Against torch.nn.functional.rms_norm (fp64) for the three norms -- gain gamma_q on
+    the query, gamma_k on the keys, none on the values -- followed by the numpy twin's
+    attention (complex-number RoPE, dense softmax)."""
+    cases = [(1, 7, 7, 4, 2, 16, 0, dict(base=1e4), 1.0),
+             (1, 5, 9, 4, 1, 32, 4, dict(base=1e6, rotate_fraction=0.25), 1.0),
+             (2, 6, 6, 6, 3, 8, 3, dict(base=1e6, yarn_factor=8.0), math.sqrt(1.2))]
+    eps = 1e-6
+    for n, (B, T, S, Hq, Hkv, d, W, rs, amp) in enumerate(cases):
+        q = _bf16((B, Hq, T, d), 700 + n)
+        z = (_bf16((B, Hkv, S, d), 710 + n).to(torch.float32) * 3).to(torch.bfloat16)
+        gq, gk = _gains(d, 720 + n, 0.6), _gains(d, 730 + n, 0.6)
+        w = orc.inv_freq(d, **rs)
+        o, lse = orc.attention_kv_shared(q, z, q_gamma=gq, k_gamma=gk, eps=eps, window=W,
+                                         scale=1.0, w=w, amp=amp)
+        rn = torch.nn.functional.rms_norm
+        qn = rn(q.to(torch.float64), (d,), weight=torch.from_numpy(gq), eps=eps).numpy()
+        kn = rn(z.to(torch.float64), (d,), weight=torch.from_numpy(gk), eps=eps).numpy()
+        vn = rn(z.to(torch.float64), (d,), eps=eps).numpy()
+        ot, lset = twin.attention(qn, kn, vn, W, 1.0, twin.inv_freq(d, **rs), amp)
+        assert np.max(np.abs(o - ot)) < 1e-12, (n, np.max(np.abs(o - ot)))
+        assert np.max(np.abs(lse - lset)) < 1e-12, n
+
+
+def check_kv_shared_decode(orc):
+    """Decode of a shared-projection layer: with a linear cache of Z holding tokens
+    0..t-1 it gives row t of the prefill over tokens 0..t; with a ring (last W-1 kept plus
+    the new token, re-numbered) it gives windowed attention over the whole history."""
+    Hq, Hkv, d, eps = 4, 2, 16, 1e-6
+    gq, gk = _gains(d, 740, 0.7), _gains(d, 741, 0.7)
+    w = orc.inv_freq(d, 1e4)
+    for is_ring, n_before, cap in ((0, 9, 12), (1, 5, 6), (1, 15, 6), (1, 25, 6)):
+        g = torch.Generator().manual_seed(750 + n_before + 100 * is_ring)
+        hist = torch.randn(Hkv, n_before + 1, d, generator=g).to(torch.bfloat16)
+        q = torch.randn(1, Hq, d, generator=g).to(torch.bfloat16)
+        cache = torch.randn(Hkv, cap, d, generator=g).to(torch.bfloat16)   # stale slots
+        for i in range(n_before):
+            cache[:, i % cap if is_ring else i] = hist[:, i]
+        o, _, slots, after = orc.decode_step_kv_shared(
+            q, hist[:, n_before][None], [cache], [cap], [n_before], [is_ring], [w], [1.0],
+            q_gamma=gq, k_gamma=gk, eps=eps, scale=0.5)
+        assert slots[0] == (n_before % cap if is_ring else n_before)
+        assert after[0] == n_before + 1
+        Q = torch.zeros(1, Hq, n_before + 1, d, dtype=torch.bfloat16)
+        Q[0, :, n_before] = q[0]
+        of, _ = orc.attention_kv_shared(Q, hist[None], q_gamma=gq, k_gamma=gk, eps=eps,
+                                        window=cap if is_ring else 0, scale=0.5, w=w, amp=1.0)
+        assert np.max(np.abs(of[0, :, n_before] - o[0])) < 1e-9, (is_ring, n_before)
+
+
 ALL_CHECKS = [
+    check_kv_shared_library,
+    check_kv_shared_decode,
     check_rms_norm_closed_form,
     check_rms_norm_library,
     check_rms_norm_scale_invariance,

@@ -3,7 +3,8 @@
 The oracle source carries switches (-DORC_PLANT=n) that inject one plausible error each:
 1 rotation sign, 2 window one token too wide, 3 interleaved GQA groups, 4 scale dropped,
 5 wrong frequency exponent, 6 YaRN interpolation reversed, 7 ring index off by one,
-8 RMSNorm over the sum of squares instead of their mean.
+8 RMSNorm over the sum of squares instead of their mean, 9 values of a shared K/V
+projection normalised with the key gain instead of none.
 The default build plants nothing (checked here too).
 """
 import pytest
@@ -11,7 +12,7 @@ import pytest
 import oracle
 import oracle_checks
 
-PLANTS = [1, 2, 3, 4, 5, 6, 7, 8]
+PLANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9]
 
 
 def _failures(orc):
