@@ -603,9 +603,16 @@ def oracle_prefill_sample(layer, target_s: float, seed: int = 0):
                     for t in rows[:, 2])
         return dt, 4 * layer.d * pairs, n
 
-    dt, fl, n = run(16)
-    n = int(min(200000, max(16, 16 * target_s / max(dt, 1e-3))))
-    dt, fl, n = run(n)
+    # each call rotates its group's keys once, then pays per row: fit both costs from two
+    # calls, then run batches of at most 100k rows until about target_s has been spent
+    dt1, _, n1 = run(64)
+    dt2, _, n2 = run(1024)
+    per_row = max((dt2 - dt1) / (n2 - n1), 1e-7)
+    batch = int(min(100000, max(1024, (target_s - dt1) / per_row)))
+    dt = fl = n = 0
+    while dt < 0.8 * target_s:
+        d_i, f_i, n_i = run(batch)
+        dt, fl, n = dt + d_i, fl + f_i, n + n_i
     return fl / dt / 1e12, {"rows": n, "seconds": dt}
 
 
