@@ -340,7 +340,7 @@ def e2e_prefill(L, st, steps, warmup, stream, flops):
     ms = statistics.mean(a for (a,) in timer.durations_ms())
     nb = lambda t: t.numel() * t.element_size()  # noqa: E731
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": nb(qh) + nb(kh) + nb(vh), "d2h_bytes_per_step": nb(oh)}
+            "h2d_bytes_per_step": sum(nb(h) for h, _ in ins), "d2h_bytes_per_step": nb(oh)}
 
 
 # ----------------------------------------------------------------------------------------
@@ -354,7 +354,9 @@ def decode_setup(w):
     from workloads import decode_inputs
     x = decode_inputs(w)
     st = {"x": x, "q": x.q.cuda(), "k_new": x.k_new.cuda(), "v_new": x.v_new.cuda(),
-          "kc": [t.cuda() for t in x.k_cache], "vc": [t.cuda() for t in x.v_cache]}
+          "kc": [t.cuda() for t in x.k_cache]}
+    # a shared K/V layer has one cache per sequence (its descriptors' v is never read)
+    st["vc"] = st["kc"] if w.kv_shared else [t.cuda() for t in x.v_cache]
     tables = {}
     for r in set(x.rope):
         n = max(x.cap[i] for i in range(w.nseq) if x.rope[i] == r)
@@ -374,7 +376,37 @@ def decode_setup(w):
     st["ws"] = torch.empty(st["wsb"], dtype=torch.uint8, device="cuda")
     st["retained"] = [min(c + 1, cap) if ring else c + 1
                       for c, cap, ring in zip(x.count_before, x.cap, x.is_ring)]
+    if w.kv_shared:
+        # one cache per sequence holding Zn = N_1(Z) of the drawn rows (normalised once,
+        # untimed); the query and key gains of the layer
+        from workloads import norm_gains
+        for i, zc in enumerate(st["kc"]):
+            gqa.gqa_qk_norm_rope_kv_shared(None, zc, None, zc, None, 1, 0, w.Hkv, x.cap[i], w.d,
+                                           0, None, None, 1e-6, None, 0)
+        st["q_gamma"] = torch.from_numpy(norm_gains(w.d, w.seed + 1)).float().cuda()
+        st["k_gamma"] = torch.from_numpy(norm_gains(w.d, w.seed + 2)).float().cuda()
+        st["q_out"] = torch.empty_like(st["q"])
     return st
+
+
+def decode_step_calls(w, st, stream, mark=None):
+    """The step's two calls: append the new token (plain K/V, or the shared projection's
+    normalised row plus the normalised query), then the decode attention."""
+    import global_causal_gqa_gb300 as gqa
+    mark = mark or (lambda: None)
+    if w.kv_shared:
+        gqa.gqa_kv_shared_append(st["descs"], w.nseq, st["q"], st["k_new"], w.Hq, w.Hkv, w.d,
+                                 st["q_gamma"], 1e-6, st["q_out"], None, stream)
+        mark()
+        gqa.gqa_attn_decode_kv_shared(st["q_out"], st["descs"], w.nseq, w.Hq, w.Hkv, w.d,
+                                      w.scale, st["k_gamma"], st["max_len"], st["o"], None,
+                                      st["ws"], st["wsb"], stream)
+    else:
+        gqa.gqa_kv_append(st["descs"], w.nseq, st["k_new"], st["v_new"], w.Hkv, w.d, None,
+                          stream)
+        mark()
+        gqa.gqa_attn_decode(st["q"], st["descs"], w.nseq, w.Hq, w.Hkv, w.d, w.scale,
+                            st["max_len"], st["o"], None, st["ws"], st["wsb"], stream)
 
 
 def bench_decode(w, steps, warmup, stream, peaks, peak_src, world, with_e2e, clocks_index=None):
@@ -382,7 +414,7 @@ def bench_decode(w, steps, warmup, stream, peaks, peak_src, world, with_e2e, clo
     import global_causal_gqa_gb300 as gqa
     from global_causal_gqa_gb300 import accounting as acc
     st = decode_setup(w)
-    kv_bytes = acc.decode_kv_bytes(st["retained"], w.Hkv, w.d)
+    kv_bytes = acc.decode_kv_bytes(st["retained"], w.Hkv, w.d, kv_shared=w.kv_shared)
     qo_bytes = 2 * w.nseq * w.Hq * w.d * 2
     timer = Timer(torch, stream, 3)
 
@@ -390,11 +422,7 @@ def bench_decode(w, steps, warmup, stream, peaks, peak_src, world, with_e2e, clo
         # every step starts from the same cache state (descriptor counts restored, untimed)
         st["descs"].copy_(st["descs0"], non_blocking=True)
         mark()
-        gqa.gqa_kv_append(st["descs"], w.nseq, st["k_new"], st["v_new"], w.Hkv, w.d, None,
-                          stream)
-        mark()
-        gqa.gqa_attn_decode(st["q"], st["descs"], w.nseq, w.Hq, w.Hkv, w.d, w.scale,
-                            st["max_len"], st["o"], None, st["ws"], st["wsb"], stream)
+        decode_step_calls(w, st, stream, mark)
         mark()
 
     timer.run(warmup, step, timed=False)
@@ -439,20 +467,21 @@ def e2e_decode(w, st, steps, warmup, stream, kv_bytes):
     import torch
     import global_causal_gqa_gb300 as gqa
     x = st["x"]
-    qh, kh, vh = (t.pin_memory() for t in (x.q, x.k_new, x.v_new))
+    # host inputs of one step: the query and the new token's rows (K and V, or the shared
+    # projection's Z alone)
+    ins = [(x.q, st["q"]), (x.k_new, st["k_new"])]
+    if not w.kv_shared:
+        ins.append((x.v_new, st["v_new"]))
+    ins = [(h.pin_memory(), dev) for h, dev in ins]
     oh = torch.empty_like(x.q).pin_memory()
     timer = Timer(torch, stream, 2)
 
     def step(mark):
         st["descs"].copy_(st["descs0"], non_blocking=True)
         mark()
-        st["q"].copy_(qh, non_blocking=True)
-        st["k_new"].copy_(kh, non_blocking=True)
-        st["v_new"].copy_(vh, non_blocking=True)
-        gqa.gqa_kv_append(st["descs"], w.nseq, st["k_new"], st["v_new"], w.Hkv, w.d, None,
-                          stream)
-        gqa.gqa_attn_decode(st["q"], st["descs"], w.nseq, w.Hq, w.Hkv, w.d, w.scale,
-                            st["max_len"], st["o"], None, st["ws"], st["wsb"], stream)
+        for h, dev in ins:
+            dev.copy_(h, non_blocking=True)
+        decode_step_calls(w, st, stream)
         oh.copy_(st["o"], non_blocking=True)
         mark()
 
@@ -461,7 +490,7 @@ def e2e_decode(w, st, steps, warmup, stream, kv_bytes):
     ms = statistics.mean(a for (a,) in timer.durations_ms())
     nb = lambda t: t.numel() * t.element_size()  # noqa: E731
     return {"value": kv_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": nb(qh) + nb(kh) + nb(vh), "d2h_bytes_per_step": nb(oh)}
+            "h2d_bytes_per_step": sum(nb(h) for h, _ in ins), "d2h_bytes_per_step": nb(oh)}
 
 
 # ----------------------------------------------------------------------------------------
@@ -630,16 +659,26 @@ def oracle_decode_sample(w, target_s: float, seed: int = 0):
                        r.rotate_fraction) for r in x.rope]
     order = list(range(w.nseq - 1, -1, -1))   # rings first, then global sequences
 
+    if w.kv_shared:
+        from workloads import norm_gains
+        gq, gk = norm_gains(w.d, w.seed + 1), norm_gains(w.d, w.seed + 2)
+
     def run(idx):
         sub = lambda a: [a[i] for i in idx]  # noqa: E731
         t0 = time.perf_counter()
-        orc.decode_step(x.q[idx], x.k_new[idx], x.v_new[idx], sub(x.k_cache), sub(x.v_cache),
-                        sub(x.cap), sub(x.count_before), sub(x.is_ring), sub(ws),
-                        [r.amp for r in sub(x.rope)], w.scale)
+        if w.kv_shared:
+            orc.decode_step_kv_shared(x.q[idx], x.k_new[idx], sub(x.k_cache), sub(x.cap),
+                                      sub(x.count_before), sub(x.is_ring), sub(ws),
+                                      [r.amp for r in sub(x.rope)], q_gamma=gq, k_gamma=gk,
+                                      eps=1e-6, scale=w.scale)
+        else:
+            orc.decode_step(x.q[idx], x.k_new[idx], x.v_new[idx], sub(x.k_cache),
+                            sub(x.v_cache), sub(x.cap), sub(x.count_before), sub(x.is_ring),
+                            sub(ws), [r.amp for r in sub(x.rope)], w.scale)
         dt = time.perf_counter() - t0
         ret = [min(x.count_before[i] + 1, x.cap[i]) if x.is_ring[i] else x.count_before[i] + 1
                for i in idx]
-        return dt, acc.decode_kv_bytes(ret, w.Hkv, w.d)
+        return dt, acc.decode_kv_bytes(ret, w.Hkv, w.d, kv_shared=w.kv_shared)
 
     dt, b = run(order[:1])
     k = 1
@@ -699,6 +738,7 @@ def config_of(wl):
         return {"workload": wl.name, "nseq": wl.nseq, "n_global": wl.n_global,
                 "n_local": wl.n_local, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
                 "global_len": list(wl.global_len_range), "window": wl.window,
+                "kv_shared": wl.kv_shared, "scale": wl.scale,
                 "l2": "flushed before every timed step (256 MiB write)"}
     L = wl.layers[0]
     cfg = {"workload": wl.name, "layers": len(wl.layers), "B": L.B, "T": L.T, "S": L.S,
@@ -762,7 +802,8 @@ def main():
     extra = []
     if world == 1 and not args.no_extra:
         for name in ("plamo3_local_prefill", "plamo3_global_prefill", "plamo3_decode_batch32",
-                     "gemma4_period_6layer", "gemma4_decode_global", "gemma4_decode_local",
+                     "gemma4_period_6layer", "gemma4_decode_global",
+                     "gemma4_decode_global_kv_shared", "gemma4_decode_local",
                      "plamo3_decode_64layer"):
             if name == wl.name:
                 continue

@@ -84,6 +84,10 @@ def lib() -> ctypes.CDLL:
             "gqa_kv_append_chunk": ([P, I, P, P, I, I, I, P], I),
             "gqa_qk_norm_rope": ([P, P, P, P, P, I, I, I, I, I, I, P, P, F, P, I, P], I),
             "gqa_qk_norm_append": ([P, I, P, P, P, I, I, I, P, P, F, I, P, P, P], I),
+            "gqa_qk_norm_rope_kv_shared": ([P, P, P, P, P, I, I, I, I, I, I, P, P, F, P, I, P],
+                                           I),
+            "gqa_kv_shared_append": ([P, I, P, P, I, I, I, P, F, P, P, P], I),
+            "gqa_attn_decode_kv_shared": ([P, P, I, I, I, I, F, P, I, P, P, P, Z, P], I),
             "gqa_get_device_status": ([P], I),
             "gqa_get_device_diag": ([P, P, I], I),
             "gqa_watchdog_selftest": ([ctypes.c_int64, P], I),
@@ -253,6 +257,36 @@ def gqa_qk_norm_append(descs, nseq: int, q, k_new, v_new, Hq: int, Hkv: int, d: 
                                   d, _ptr(q_gamma), _ptr(k_gamma), eps, v_norm, _ptr(q_out),
                                   _ptr(slots_out), _stream(stream))
     return _check("gqa_qk_norm_append", st, check)
+
+
+# ---- shared K/V projection (Gemma 4 global layers) ---------------------------------------
+
+def gqa_qk_norm_rope_kv_shared(q, z, q_out, v_out, k_rot, B: int, Hq: int, Hkv: int, T: int,
+                               d: int, pos0: int, q_gamma, k_gamma, eps: float, table,
+                               table_len: int, stream=None, check: bool = True) -> int:
+    st = lib().gqa_qk_norm_rope_kv_shared(_ptr(q), _ptr(z), _ptr(q_out), _ptr(v_out),
+                                          _ptr(k_rot), B, Hq, Hkv, T, d, pos0, _ptr(q_gamma),
+                                          _ptr(k_gamma), eps, _ptr(table), table_len,
+                                          _stream(stream))
+    return _check("gqa_qk_norm_rope_kv_shared", st, check)
+
+
+def gqa_kv_shared_append(descs, nseq: int, q, z_new, Hq: int, Hkv: int, d: int, q_gamma,
+                         eps: float, q_out, slots_out=None, stream=None,
+                         check: bool = True) -> int:
+    st = lib().gqa_kv_shared_append(_ptr(descs), nseq, _ptr(q), _ptr(z_new), Hq, Hkv, d,
+                                    _ptr(q_gamma), eps, _ptr(q_out), _ptr(slots_out),
+                                    _stream(stream))
+    return _check("gqa_kv_shared_append", st, check)
+
+
+def gqa_attn_decode_kv_shared(q, descs, nseq: int, Hq: int, Hkv: int, d: int, scale: float,
+                              k_gamma, max_len: int, o, lse, workspace, workspace_bytes: int,
+                              stream=None, check: bool = True) -> int:
+    st = lib().gqa_attn_decode_kv_shared(_ptr(q), _ptr(descs), nseq, Hq, Hkv, d, scale,
+                                         _ptr(k_gamma), max_len, _ptr(o), _ptr(lse),
+                                         _ptr(workspace), workspace_bytes, _stream(stream))
+    return _check("gqa_attn_decode_kv_shared", st, check)
 
 
 # ---- status ---------------------------------------------------------------------------------

@@ -35,9 +35,12 @@ def prefill_flops(B: int, Hq: int, T: int, S: int, d: int, window: int) -> int:
     return 4 * d * B * Hq * unmasked_pairs(T, S, window)
 
 
-def decode_kv_bytes(retained: Iterable[int], Hkv: int, d: int, elem_bytes: int = 2) -> int:
-    """K and V bytes one decode step must read: 2 Hkv d elem_bytes per retained token."""
-    return sum(2 * int(r) * Hkv * d * elem_bytes for r in retained)
+def decode_kv_bytes(retained: Iterable[int], Hkv: int, d: int, elem_bytes: int = 2,
+                    kv_shared: bool = False) -> int:
+    """K and V bytes one decode step must read: 2 Hkv d elem_bytes per retained token, or
+    half that when K and V share one cached row (Gemma 4 global layers)."""
+    rows = 1 if kv_shared else 2
+    return sum(rows * int(r) * Hkv * d * elem_bytes for r in retained)
 
 
 def kv_bytes_per_token(L: int, Hkv: int, d: int, N: int, W: int, elem_bytes: int = 2) -> int:

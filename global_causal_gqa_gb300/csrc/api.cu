@@ -222,7 +222,28 @@ gqa_status gqa_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_o
         return GQA_ERR_ALIGNMENT;
     if (k_rot && (long)pos0 + T > (long)table_len) return GQA_ERR_RANGE;
     return from_cuda(gqa::launch_qk_norm_rope(q, k, q_out, k_out, k_rot, B, Hq, Hkv, T, d, pos0,
-                                              q_gamma, k_gamma, eps, table,
+                                              q_gamma, k_gamma, eps, table, 0,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_qk_norm_rope_kv_shared(const void *q, const void *z, void *q_out, void *v_out,
+                                      void *k_rot, int B, int Hq, int Hkv, int T, int d,
+                                      int pos0, const float *q_gamma, const float *k_gamma,
+                                      float eps, const float *table, int table_len,
+                                      gqa_stream_t stream) {
+    const bool with_q = q != nullptr;
+    if (!z || (with_q && (!q_out || !q_gamma || Hq <= 0)) || (!with_q && q_out) ||
+        (!v_out && !k_rot) || (k_rot && (!k_gamma || !table)) || B <= 0 || Hkv <= 0 ||
+        T <= 0 || pos0 < 0 || !(eps >= 0.f) || !std::isfinite(eps))
+        return GQA_ERR_INVALID_ARG;
+    if (!rope_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
+    if ((with_q && (!aligned16(q) || !aligned16(q_out) || !aligned16(q_gamma))) ||
+        !aligned16(z) || (v_out && !aligned16(v_out)) || (k_rot && !aligned16(k_rot)) ||
+        (k_gamma && !aligned16(k_gamma)) || (table && !aligned16(table)))
+        return GQA_ERR_ALIGNMENT;
+    if (k_rot && (long)pos0 + T > (long)table_len) return GQA_ERR_RANGE;
+    return from_cuda(gqa::launch_qk_norm_rope(q, z, q_out, v_out, k_rot, B, with_q ? Hq : 0, Hkv,
+                                              T, d, pos0, q_gamma, k_gamma, eps, table, 1,
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -242,6 +263,23 @@ gqa_status gqa_qk_norm_append(gqa_kv_desc *descs, int nseq, const void *q, const
     if (!st) return GQA_ERR_CUDA;
     return from_cuda(gqa::launch_qk_norm_append(descs, nseq, q, k_new, v_new, Hq, Hkv, d, q_gamma,
                                                 k_gamma, eps, v_norm, q_out, slots_out, st,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_kv_shared_append(gqa_kv_desc *descs, int nseq, const void *q, const void *z_new,
+                                int Hq, int Hkv, int d, const float *q_gamma, float eps,
+                                void *q_out, int32_t *slots_out, gqa_stream_t stream) {
+    if (!descs || !q || !z_new || !q_out || !q_gamma || nseq <= 0 || Hq <= 0 || Hkv <= 0 ||
+        !(eps >= 0.f) || !std::isfinite(eps))
+        return GQA_ERR_INVALID_ARG;
+    if (!rope_dim_ok(d)) return GQA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(z_new) || !aligned16(q_out) || !aligned16(q_gamma) ||
+        (reinterpret_cast<uintptr_t>(descs) & 7u))
+        return GQA_ERR_ALIGNMENT;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    return from_cuda(gqa::launch_qk_norm_append(descs, nseq, q, z_new, nullptr, Hq, Hkv, d,
+                                                q_gamma, nullptr, eps, 0, q_out, slots_out, st,
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -270,6 +308,29 @@ gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, in
     return from_cuda(gqa::launch_decode(q, descs, nseq, Hq, Hkv, d, scale, max_len, o, lse,
                                         static_cast<float *>(workspace), st,
                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gqa_status gqa_attn_decode_kv_shared(const void *q, const gqa_kv_desc *descs, int nseq, int Hq,
+                                     int Hkv, int d, float scale, const float *k_gamma,
+                                     int max_len, void *o, float *lse, void *workspace,
+                                     size_t workspace_bytes, gqa_stream_t stream) {
+    if (!q || !descs || !o || !k_gamma || nseq <= 0 || Hq <= 0 || Hkv <= 0 ||
+        (Hq % Hkv) != 0 || max_len <= 0 || !std::isfinite(scale))
+        return GQA_ERR_INVALID_ARG;
+    if ((d != 128 && d != 256 && d != 512) || Hq / Hkv > 8) return GQA_ERR_UNSUPPORTED;
+    if (nseq > 65535) return GQA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(o) || !aligned16(k_gamma) ||
+        (reinterpret_cast<uintptr_t>(descs) & 7u) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return GQA_ERR_ALIGNMENT;
+    const size_t need = gqa_decode_workspace_bytes(nseq, Hq, d, max_len);
+    if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GQA_ERR_ALIGNMENT;
+    int *st = status_ptr();
+    if (!st) return GQA_ERR_CUDA;
+    return from_cuda(gqa::launch_decode(q, descs, nseq, Hq, Hkv, d, scale, max_len, o, lse,
+                                        static_cast<float *>(workspace), st,
+                                        reinterpret_cast<cudaStream_t>(stream), k_gamma));
 }
 
 // ---- decode with library-owned scratch (no allocation) ---------------------------------

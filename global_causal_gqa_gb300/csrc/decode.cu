@@ -21,6 +21,12 @@
 // RoPE pair (j, j + 64) sits in one thread.  K is rotated in registers from the fp32
 // table at its logical position.  Each warp writes an unnormalised partial (m, l, O) for
 // its G heads; the combine kernel merges the splits by their log-sum-exp.
+//
+// Shared K/V projection (Gemma 4 global layers, attention_k_eq_v, §5.2 and §8 of the same
+// page): the cache holds one row Zn = N_1(Z) per token; the values are Zn and the keys
+// RoPE(bf16(gamma_k) * Zn), the gain applied in bf16 to each loaded K fragment before the
+// rotation.  The V fragments are loaded from the same rows, so HBM delivers each row once
+// (the second read of a line is served by L2): half the bytes of separate K and V.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -129,13 +135,30 @@ __device__ __forceinline__ SeqView seq_view(const gqa_kv_desc &desc, int max_len
     return v;
 }
 
-template <int PARTS>   // warps per KV head: d = 128 PARTS
+// Shared memory after the table stages and the exchange: the key gain as bf16 pairs.
+constexpr int kDecodeSmemShared = kDecodeSmem + kMaxHeadDim * 2;
+
+__device__ __forceinline__ uint4 mul_bf16x8(const uint4 &a, const uint4 &b) {
+    return make_uint4(mul_bf16x2(a.x, b.x), mul_bf16x2(a.y, b.y), mul_bf16x2(a.z, b.z),
+                      mul_bf16x2(a.w, b.w));
+}
+
+template <int PARTS, bool SHARED>   // warps per KV head: d = 128 PARTS; shared K/V rows
 __global__ void __launch_bounds__(kWarps * 32, 1)
     decode_partial_kernel(const __nv_bfloat16 *__restrict__ q,
                           const gqa_kv_desc *__restrict__ descs, int Hq, int Hkv,
                           float scale_log2, int max_len, int nsplit, float *__restrict__ ws_ml,
-                          float *__restrict__ ws_o, int *status) {
+                          float *__restrict__ ws_o, int *status,
+                          const float *__restrict__ k_gamma) {
     constexpr int d = kD * PARTS, parts = PARTS;
+    extern __shared__ float4 dsmem[];
+    uint4 *sgain = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(dsmem) + kDecodeSmem);
+    if constexpr (SHARED) {
+        // before any warp may leave: every thread takes part in the barrier
+        for (int i = threadIdx.x; i < d / 2; i += blockDim.x)
+            reinterpret_cast<uint32_t *>(sgain)[i] = pack_bf16x2(k_gamma[2 * i], k_gamma[2 * i + 1]);
+        __syncthreads();
+    }
     const int split = blockIdx.x, seq = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int part = warp % parts;               // this warp's RoPE pairs: [64 part, +64)
@@ -198,13 +221,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     // (k, lane) at k * 32 + (lane ^ 2 (k & 3)) holding what lane (gq, tq) needs for
     // k = 8 rs + 4 c + qq: pairs 32c + 8tq + 2qq and the next one at position kb + gq + 8 rs.
     // The XOR keeps both the copies in and the reads out free of bank conflicts.
-    extern __shared__ float4 dsmem[];
     float4 *stage_base = dsmem + (size_t)warp * 2 * 512;
     float *xchg = reinterpret_cast<float *>(dsmem + (size_t)kWarps * 2 * 512) +
                   (size_t)hg * (2 * parts * 32 * 4);
 
     const __nv_bfloat16 *kbase = static_cast<const __nv_bfloat16 *>(desc.k) + (size_t)g * sv.cap * d;
-    const __nv_bfloat16 *vbase = static_cast<const __nv_bfloat16 *>(desc.v) + (size_t)g * sv.cap * d;
+    const __nv_bfloat16 *vbase =
+        SHARED ? kbase : static_cast<const __nv_bfloat16 *>(desc.v) + (size_t)g * sv.cap * d;
     auto slot_of = [&](int key) {
         int s = sv.first + key;
         return s >= sv.cap ? s - sv.cap : s;
@@ -263,6 +286,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         else cp_async_wait<0>();
         __syncwarp();
         const float4 *stg = stage_base + (((kb - k_start) >> 4) & 1) * 512;
+        if constexpr (SHARED) {
+            // keys = bf16(gamma_k) * Zn before the rotation; chunk lc holds elements
+            // 8 gchunk(lc) .. + 7 in order, as does word group gchunk(lc) of the gain
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint4 gw = sgain[gchunk(4 * c + tq)];
+                bl.k0[c] = mul_bf16x8(bl.k0[c], gw);
+                bl.k1[c] = mul_bf16x8(bl.k1[c], gw);
+            }
+        }
         // rotate K at logical positions kb + gq, kb + gq + 8 (clamped rows: k_end - 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -417,7 +450,7 @@ int decode_num_splits(int max_len) {
 
 cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
                           int d, float scale, int max_len, void *o, float *lse, float *ws,
-                          int *status, cudaStream_t s) {
+                          int *status, cudaStream_t s, const float *k_gamma) {
     const int nsplit = decode_num_splits(max_len);
     float *ws_ml = ws;
     float *ws_o = ws + (size_t)2 * nseq * Hq * nsplit;
@@ -428,20 +461,28 @@ cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int
     const float scale_log2 = scale * 1.4426950408889634f;
     static bool attr_done = false;
     if (!attr_done) {
-        for (const void *f : {reinterpret_cast<const void *>(decode_partial_kernel<1>),
-                              reinterpret_cast<const void *>(decode_partial_kernel<2>),
-                              reinterpret_cast<const void *>(decode_partial_kernel<4>)}) {
-            const cudaError_t e =
-                cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+        for (const void *f : {reinterpret_cast<const void *>(decode_partial_kernel<1, false>),
+                              reinterpret_cast<const void *>(decode_partial_kernel<2, false>),
+                              reinterpret_cast<const void *>(decode_partial_kernel<4, false>),
+                              reinterpret_cast<const void *>(decode_partial_kernel<1, true>),
+                              reinterpret_cast<const void *>(decode_partial_kernel<2, true>),
+                              reinterpret_cast<const void *>(decode_partial_kernel<4, true>)}) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmemShared);
             if (e != cudaSuccess) return e;
         }
         attr_done = true;
     }
-    auto kern = parts == 1 ? decode_partial_kernel<1>
-                : parts == 2 ? decode_partial_kernel<2> : decode_partial_kernel<4>;
-    kern<<<grid, heads * parts * 32, kDecodeSmem, s>>>(
+    const bool shared = k_gamma != nullptr;
+    auto kern = shared ? (parts == 1   ? decode_partial_kernel<1, true>
+                          : parts == 2 ? decode_partial_kernel<2, true>
+                                       : decode_partial_kernel<4, true>)
+                       : (parts == 1   ? decode_partial_kernel<1, false>
+                          : parts == 2 ? decode_partial_kernel<2, false>
+                                       : decode_partial_kernel<4, false>);
+    kern<<<grid, heads * parts * 32, shared ? kDecodeSmemShared : kDecodeSmem, s>>>(
         static_cast<const __nv_bfloat16 *>(q), descs, Hq, Hkv, scale_log2, max_len, nsplit,
-        ws_ml, ws_o, status);
+        ws_ml, ws_o, status, k_gamma);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     decode_combine_kernel<<<dim3(Hq, nseq), d, 0, s>>>(descs, Hq, d, max_len, nsplit, ws_ml,

@@ -33,9 +33,12 @@ __host__ __device__ inline int decode_chunk(int max_len) {
     return max_len > 4096 ? kDecodeChunkLong : kDecodeChunkShort;
 }
 int decode_num_splits(int max_len);
+// k_gamma == nullptr: separate K and V caches; otherwise each desc.k holds Zn of a shared
+// K/V projection (keys RoPE(bf16(gamma_k) * Zn), values Zn) and desc.v is not read
 cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
                           int d, float scale, int max_len, void *o, float *lse,
-                          float *ws, int *status, cudaStream_t s);
+                          float *ws, int *status, cudaStream_t s,
+                          const float *k_gamma = nullptr);
 
 // d = 128 prefill: picks the persistent kernel (prefill.cu) or the one-CTA-per-item
 // kernel (prefill_stream.cu) by the mean item length; returns a gqa_status
@@ -66,7 +69,7 @@ cudaError_t launch_kv_append_chunk(gqa_kv_desc *descs, int nseq, const void *k_n
 cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out,
                                 void *k_rot, int B, int Hq, int Hkv, int T, int d, int pos0,
                                 const float *q_gamma, const float *k_gamma, float eps,
-                                const float *table, cudaStream_t s);
+                                const float *table, int kv_shared, cudaStream_t s);
 cudaError_t launch_qk_norm_append(gqa_kv_desc *descs, int nseq, const void *q, const void *k_new,
                                   const void *v_new, int Hq, int Hkv, int d,
                                   const float *q_gamma, const float *k_gamma, float eps,

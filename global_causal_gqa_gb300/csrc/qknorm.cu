@@ -9,6 +9,12 @@
 // RMSNorm to V (§8 of the same page).  The sums of squares and the scaling run in fp32;
 // each output is rounded once to bf16.
 //
+// Shared K/V projection (Gemma 4 global layers, attention_k_eq_v, §5.2 and §8): one
+// projection output Z gives K = RoPE(N_{gamma_k}(Z)) and V = N_1(Z).  The cache stores
+// only Zn = bf16(N_1(Z)); since N_gamma(Z) = gamma * N_1(Z), the keys are recomputed from
+// it as RoPE(bf16(bf16(gamma_k) * Zn)) -- the gain applied in bf16 to the stored row,
+// exactly as the decode kernel applies it -- so prefill and decode see the same keys.
+//
 // One warp per row.  Lane l holds the 32-bit words (bf16 pairs) l, l + 32, ... of the
 // row's first half and the words d/4 later of the second half, so each RoPE pair
 // (j, j + d/2) sits in one lane; loads and stores are 4-byte and coalesced per warp.
@@ -84,13 +90,43 @@ __device__ __forceinline__ void finish_row(const Row &row, int d, int lane, floa
     }
 }
 
+// Shared K/V row: Zn = bf16(x * inv) to `v_out` (nullable); the key row
+// RoPE(bf16(bf16(gamma) * Zn)) by the table row `tab` to `k_rot` (nullable).
+__device__ __forceinline__ void finish_row_shared(const Row &row, int d, int lane, float inv,
+                                                  const float *gamma, uint32_t *v_out,
+                                                  uint32_t *k_rot, const float2 *tab) {
+    const int hw = d / 4;
+#pragma unroll
+    for (int m = 0; m < kMaxWordsPerLane / 2; ++m) {
+        const int w = lane + 32 * m;
+        if (w < hw) {
+            const uint32_t za = pack_bf16x2(bf16lo(row.a[m]) * inv, bf16hi(row.a[m]) * inv);
+            const uint32_t zb = pack_bf16x2(bf16lo(row.b[m]) * inv, bf16hi(row.b[m]) * inv);
+            if (v_out) {
+                v_out[w] = za;
+                v_out[w + hw] = zb;
+            }
+            if (k_rot) {
+                const float2 ga = gain2(gamma, w), gb = gain2(gamma, w + hw);
+                const uint32_t ka = mul_bf16x2(za, pack_bf16x2(ga.x, ga.y));
+                const uint32_t kb = mul_bf16x2(zb, pack_bf16x2(gb.x, gb.y));
+                const float a0 = bf16lo(ka), a1 = bf16hi(ka), b0 = bf16lo(kb), b1 = bf16hi(kb);
+                const float4 t = reinterpret_cast<const float4 *>(tab)[w];
+                k_rot[w] = pack_bf16x2(a0 * t.x - b0 * t.y, a1 * t.z - b1 * t.w);
+                k_rot[w + hw] = pack_bf16x2(a0 * t.y + b0 * t.x, a1 * t.w + b1 * t.z);
+            }
+        }
+    }
+}
+
 // Prefill: Q rows [rows_q, d] -> q_out = N_q(q); K rows [rows_k, d] (row = (b, g, t)) ->
-// k_out = N_k(k), k_rot = RoPE(N_k(k)) at position pos0 + t.
+// k_out = N_k(k), k_rot = RoPE(N_k(k)) at position pos0 + t; with kv_shared the K rows are
+// shared projection outputs Z: k_out = Zn (the values and the cache row), k_rot as above.
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(
     const uint32_t *__restrict__ q, const uint32_t *__restrict__ k, uint32_t *q_out,
     uint32_t *k_out, uint32_t *k_rot, long rows_q, long rows_k, int T, int d, int pos0,
     const float *__restrict__ q_gamma, const float *__restrict__ k_gamma, float eps,
-    const float2 *__restrict__ table) {
+    const float2 *__restrict__ table, int kv_shared) {
     const int lane = threadIdx.x & 31;
     const long warps = (long)gridDim.x * (blockDim.x >> 5);
     const int wpr = d / 2;   // words per row
@@ -105,9 +141,15 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(
             const long rk = r - rows_q;
             const int t = static_cast<int>(rk % T);
             const float ss = warp_sum(load_row(k + rk * wpr, d, lane, row));
-            finish_row(row, d, lane, rsqrtf(ss / d + eps), k_gamma,
-                       k_out ? k_out + rk * wpr : nullptr, k_rot ? k_rot + rk * wpr : nullptr,
-                       table + (size_t)(pos0 + t) * (d / 2));
+            const float2 *tab = table ? table + (size_t)(pos0 + t) * (d / 2) : nullptr;
+            if (kv_shared)
+                finish_row_shared(row, d, lane, rsqrtf(ss / d + eps), k_gamma,
+                                  k_out ? k_out + rk * wpr : nullptr,
+                                  k_rot ? k_rot + rk * wpr : nullptr, tab);
+            else
+                finish_row(row, d, lane, rsqrtf(ss / d + eps), k_gamma,
+                           k_out ? k_out + rk * wpr : nullptr,
+                           k_rot ? k_rot + rk * wpr : nullptr, tab);
         }
     }
 }
@@ -115,6 +157,8 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(
 // Decode: one block per sequence.  The new token's slot is taken as kv_append takes it;
 // Q rows are normalised into q_out, K rows normalised into the cache slot, V rows copied
 // (or, with v_norm, normalised without a gain) into the cache slot, then count += 1.
+// Shared K/V (v_new == nullptr, k_gamma == nullptr): the K rows are projection outputs Z and
+// the K cache slot receives Zn = N_1(Z); no V cache is written.
 __global__ void __launch_bounds__(256) qk_norm_append_kernel(
     gqa_kv_desc *descs, const uint32_t *__restrict__ q, const uint32_t *__restrict__ k_new,
     const uint32_t *__restrict__ v_new, int Hq, int Hkv, int d, const float *__restrict__ q_gamma,
@@ -139,7 +183,8 @@ __global__ void __launch_bounds__(256) qk_norm_append_kernel(
     const long cap = desc->cap;
     uint32_t *kc = static_cast<uint32_t *>(desc->k), *vc = static_cast<uint32_t *>(desc->v);
     const int nw = blockDim.x >> 5;
-    for (int r = warp; r < Hq + 2 * Hkv; r += nw) {
+    const int n_rows = Hq + (v_new ? 2 : 1) * Hkv;
+    for (int r = warp; r < n_rows; r += nw) {
         Row row;
         if (r < Hq) {
             const long src = ((long)seq * Hq + r) * wpr;
@@ -172,15 +217,15 @@ __global__ void __launch_bounds__(256) qk_norm_append_kernel(
 cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out,
                                 void *k_rot, int B, int Hq, int Hkv, int T, int d, int pos0,
                                 const float *q_gamma, const float *k_gamma, float eps,
-                                const float *table, cudaStream_t s) {
-    const long rows_q = (long)B * Hq * T, rows_k = (long)B * Hkv * T;
+                                const float *table, int kv_shared, cudaStream_t s) {
+    const long rows_q = q ? (long)B * Hq * T : 0, rows_k = (long)B * Hkv * T;
     long blocks = (rows_q + rows_k + 7) / 8;
     if (blocks > 152L * 16) blocks = 152L * 16;
     qk_norm_rope_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         static_cast<const uint32_t *>(q), static_cast<const uint32_t *>(k),
         static_cast<uint32_t *>(q_out), static_cast<uint32_t *>(k_out),
         static_cast<uint32_t *>(k_rot), rows_q, rows_k, T, d, pos0, q_gamma, k_gamma, eps,
-        reinterpret_cast<const float2 *>(table));
+        reinterpret_cast<const float2 *>(table), kv_shared);
     return cudaGetLastError();
 }
 

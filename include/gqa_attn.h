@@ -198,6 +198,42 @@ gqa_status gqa_qk_norm_append(gqa_kv_desc *descs, int nseq, const void *q, const
                               const float *k_gamma, float eps, int v_norm, void *q_out,
                               int32_t *slots_out, gqa_stream_t stream);
 
+/* ---- Shared K/V projection (Gemma 4 global layers) ---------------------------------------
+ * attention_k_eq_v ("PLaMo 3..." §5.2 and the Gemma 4 comparison of §8): one projection
+ * output Z [.., Hkv, .., d] per token gives both K = RoPE(N_{gamma_k}(Z)) and V = N_1(Z),
+ * N_1 being RMSNorm without a gain (eps as above).  Such a layer needs to cache only
+ * Zn = N_1(Z): since N_gamma(Z) = gamma * N_1(Z), the keys are recomputed from it.  The
+ * library does exactly that, in bf16: the stored row is Zn rounded once to bf16, and the
+ * key is RoPE(bf16(bf16(gamma_k) * Zn)) -- the gain rounded to bf16 and multiplied into
+ * the stored row with one rounding -- in prefill and decode alike.  Gains are device fp32
+ * [d], 16-byte aligned, one per layer, shared by every head; d in {64, 128, 256, 512}
+ * (decode: {128, 256, 512}).
+ *
+ * gqa_qk_norm_rope_kv_shared (prefill form): q [B, Hq, T, d] -> q_out = N_{q_gamma}(q)
+ * (rotated later, inside gqa_attn_prefill); z [B, Hkv, T, d] -> v_out = Zn (the values,
+ * and what the cache stores; nullable) and k_rot = RoPE(bf16(gamma_k) * Zn) at positions
+ * pos0 + t (nullable; pass it to gqa_attn_prefill with k_is_rotated = 1 and v_out as v).
+ * q, q_out and q_gamma may all be NULL (then Hq is ignored) to process Z alone; at least
+ * one of v_out, k_rot must be given; k_gamma and the table are needed only for k_rot.
+ * Each output may alias its own input (q_out == q; v_out or k_rot == z), not another output.
+ *
+ * gqa_kv_shared_append (decode form): q [nseq, Hq, d] -> q_out = N_{q_gamma}(q);
+ * z_new [nseq, Hkv, d] -> Zn appended to each sequence's cache at desc.k, with the slot,
+ * count update, slots_out and GQA_ERR_CAPACITY of gqa_kv_append; desc.v is not written.
+ *
+ * gqa_attn_decode_kv_shared: as gqa_attn_decode (same arguments, workspace and results),
+ * over caches of Zn at desc.k: keys RoPE(bf16(k_gamma) * Zn) at positions 0..R-1, values
+ * Zn; desc.v is not read.  The cache rows are read once from memory for both roles, half
+ * the bytes of separate K and V caches. */
+gqa_status gqa_qk_norm_rope_kv_shared(const void *q, const void *z, void *q_out, void *v_out,
+                                      void *k_rot, int B, int Hq, int Hkv, int T, int d,
+                                      int pos0, const float *q_gamma, const float *k_gamma,
+                                      float eps, const float *table, int table_len,
+                                      gqa_stream_t stream);
+gqa_status gqa_kv_shared_append(gqa_kv_desc *descs, int nseq, const void *q, const void *z_new,
+                                int Hq, int Hkv, int d, const float *q_gamma, float eps,
+                                void *q_out, int32_t *slots_out, gqa_stream_t stream);
+
 /* ---- Decode (§4.4, §4.5) ---------------------------------------------------------------
  * One query token per sequence: q [nseq, Hq, d] bf16 at position R-1, where R = count
  * (linear) or min(count, cap) (ring) read from the descriptors (so call after
@@ -213,6 +249,11 @@ size_t gqa_decode_workspace_bytes(int nseq, int Hq, int d, int max_len);
 gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq,
                            int Hkv, int d, float scale, int max_len, void *o, float *lse,
                            void *workspace, size_t workspace_bytes, gqa_stream_t stream);
+
+gqa_status gqa_attn_decode_kv_shared(const void *q, const gqa_kv_desc *descs, int nseq, int Hq,
+                                     int Hkv, int d, float scale, const float *k_gamma,
+                                     int max_len, void *o, float *lse, void *workspace,
+                                     size_t workspace_bytes, gqa_stream_t stream);
 
 /* Decode without a caller-supplied workspace; allocates nothing.  The pages have no
  * counterpart to this entry point: it is the same computation as gqa_attn_decode (same

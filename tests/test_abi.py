@@ -109,6 +109,44 @@ def test_qk_norm_arguments_rejected_on_host():
                                   fake, None, None)) == "GQA_ERR_INVALID_ARG"
 
 
+def test_kv_shared_arguments_rejected_on_host():
+    L = gqa.lib()
+    S = gqa.STATUS_NAMES
+    f = lambda st: S.get(st, st)  # noqa: E731
+    fake = 0x10000
+    # prefill form: neither output, k_rot without its gain, q without q_out, misaligned
+    # v_out, unsupported d, a position past the table
+    assert f(L.gqa_qk_norm_rope_kv_shared(None, fake, None, None, None, 1, 0, 1, 8, 128, 0,
+                                          None, fake, 1e-6, fake, 8, None)) == "GQA_ERR_INVALID_ARG"
+    assert f(L.gqa_qk_norm_rope_kv_shared(None, fake, None, None, fake, 1, 0, 1, 8, 128, 0,
+                                          None, None, 1e-6, fake, 8, None)) == "GQA_ERR_INVALID_ARG"
+    assert f(L.gqa_qk_norm_rope_kv_shared(fake, fake, None, fake, None, 1, 2, 1, 8, 128, 0,
+                                          fake, None, 1e-6, None, 0, None)) == "GQA_ERR_INVALID_ARG"
+    assert f(L.gqa_qk_norm_rope_kv_shared(None, fake, None, fake + 8, None, 1, 0, 1, 8, 128, 0,
+                                          None, None, 1e-6, None, 0, None)) == "GQA_ERR_ALIGNMENT"
+    assert f(L.gqa_qk_norm_rope_kv_shared(None, fake, None, fake, None, 1, 0, 1, 8, 100, 0,
+                                          None, None, 1e-6, None, 0, None)) == "GQA_ERR_UNSUPPORTED"
+    assert f(L.gqa_qk_norm_rope_kv_shared(None, fake, None, None, fake, 1, 0, 1, 8, 128, 5,
+                                          None, fake, 1e-6, fake, 12, None)) == "GQA_ERR_RANGE"
+    # decode form: missing query gain, negative eps
+    assert f(L.gqa_kv_shared_append(fake, 1, fake, fake, 2, 1, 128, None, 1e-6, fake, None,
+                                    None)) == "GQA_ERR_INVALID_ARG"
+    assert f(L.gqa_kv_shared_append(fake, 1, fake, fake, 2, 1, 128, fake, -1.0, fake, None,
+                                    None)) == "GQA_ERR_INVALID_ARG"
+    # decode: no key gain, head dim 64, group of 16, too little workspace, misaligned gain
+    wsb = gqa.gqa_decode_workspace_bytes(1, 2, 128, 64)
+    assert f(L.gqa_attn_decode_kv_shared(fake, fake, 1, 2, 1, 128, 1.0, None, 64, fake, None,
+                                         fake, wsb, None)) == "GQA_ERR_INVALID_ARG"
+    assert f(L.gqa_attn_decode_kv_shared(fake, fake, 1, 2, 1, 64, 1.0, fake, 64, fake, None,
+                                         fake, wsb, None)) == "GQA_ERR_UNSUPPORTED"
+    assert f(L.gqa_attn_decode_kv_shared(fake, fake, 1, 16, 1, 128, 1.0, fake, 64, fake, None,
+                                         fake, wsb, None)) == "GQA_ERR_UNSUPPORTED"
+    assert f(L.gqa_attn_decode_kv_shared(fake, fake, 1, 2, 1, 128, 1.0, fake, 64, fake, None,
+                                         fake, wsb - 4, None)) == "GQA_ERR_WORKSPACE"
+    assert f(L.gqa_attn_decode_kv_shared(fake, fake, 1, 2, 1, 128, 1.0, fake + 4, 64, fake, None,
+                                         fake, wsb, None)) == "GQA_ERR_ALIGNMENT"
+
+
 def test_chunked_prefill_arguments_rejected_on_host():
     L = gqa.lib()
     S = gqa.STATUS_NAMES

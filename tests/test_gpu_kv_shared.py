@@ -1,0 +1,242 @@
+"""Shared K/V projection (Gemma 4 global layers, attention_k_eq_v) against the fp64 oracle.
+
+One projection output Z per token gives both K = RoPE(N_{gamma_k}(Z)) and V = N_1(Z)
+("PLaMo 3アーキテクチャ徹底解析" §5.2 and the Gemma 4 comparison of §8); the query is
+N_{gamma_q}(q), rotated.  The library caches only Zn = N_1(Z) and recomputes the keys.
+Prefill: gqa_qk_norm_rope_kv_shared, then gqa_attn_prefill over (k_rot, v_out).  Decode:
+caches of Zn made from raw Z rows by the same norm pass, then gqa_kv_shared_append and
+gqa_attn_decode_kv_shared.  The oracle computes every norm from the raw bf16 rows in
+fp64.  Scale 1 (Gemma), with gains that give logits of standard deviation ~1.
+
+Two bars.  (1) Attention parity, max abs 2e-2 / mean abs 2e-3: the GPU against the plain
+oracle attention over the bf16 tensors a shared-projection layer stores -- the oracle's
+N_{gamma_q}(q) and Zn = N_1(Z) rounded to bf16, and the keys bf16(bf16(gamma_k) Zn) --
+the same bar as every other attention test.  (2) End to end from the raw rows, against
+the definition computed in fp64 without any bf16 storage: max abs 4e-2 / mean abs 2e-3.
+The three bf16 tensors stored before attention (query, Zn, keys) each add up to 2^-9
+relative error, about doubling the plain path's logit and value errors, so the max-abs
+bar is doubled; the mean bar is kept.  Slots and counts bit-exact.
+"""
+import math
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import global_causal_gqa_gb300 as gqa
+import gpu_utils as gu
+from test_gpu_decode import LOCAL, YARN, DecodeSetup, _random_batch
+from workloads import RopeSpec, decode_inputs, get_workload, norm_gains
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-6
+PROPE = RopeSpec(base=1e6, rotate_fraction=0.25)
+
+
+def _bf(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * scale).to(torch.bfloat16)
+
+
+E2E_MAX_ABS, E2E_MEAN_ABS = 4e-2, 2e-3
+
+
+def _dev_gain(g: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(g).to(torch.float32).cuda()
+
+
+def _to_bf16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(torch.float32).to(torch.bfloat16)
+
+
+def _stored(q, z, gq, gk):
+    """The bf16 tensors a shared-projection layer stores, from the oracle's norms:
+    (query N_gq(q), keys bf16(bf16(gk) Zn) before RoPE, values Zn = N_1(z))."""
+    orc = gu.orc()
+    zn = _to_bf16(orc.rms_norm(z, None, EPS))
+    keys = (zn.float() * torch.from_numpy(gk).to(torch.bfloat16).float()).to(torch.bfloat16)
+    return _to_bf16(orc.rms_norm(q, gq, EPS)), keys, zn
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,T,window,rope", [
+    (512, 8, 2, 300, 0, PROPE),
+    (256, 8, 4, 333, 128, LOCAL),
+    (128, 8, 2, 260, 0, YARN),
+    (128, 6, 3, 200, 64, LOCAL),
+])
+def test_prefill_kv_shared(d, Hq, Hkv, T, window, rope):
+    gu.require_gpu()
+    B = 1
+    q = _bf((B, Hq, T, d), 1300 + d + T)
+    z = _bf((B, Hkv, T, d), 1400 + d + T, scale=3.0)     # any scale: the norms remove it
+    gq, gk = norm_gains(d, 1500 + d), norm_gains(d, 1600 + d)
+    table = gu.rope_table(d, rope, T)
+    qd, zd = q.cuda(), z.cuda()
+    q_out, v_out, k_rot = torch.empty_like(qd), torch.empty_like(zd), torch.empty_like(zd)
+    gqa.gqa_qk_norm_rope_kv_shared(qd, zd, q_out, v_out, k_rot, B, Hq, Hkv, T, d, 0,
+                                   _dev_gain(gq), _dev_gain(gk), EPS, table, T)
+    assert gqa.gqa_get_device_status() == 0
+    orc = gu.orc()
+    w = gu.oracle_freq(d, rope)
+    # the pass's own outputs: the values (and cache rows) Zn, the rotated keys
+    gu.compare(q_out, orc.rms_norm(q, gq, EPS), what="q_out")
+    gu.compare(v_out, orc.rms_norm(z, None, EPS), what="v_out = Zn")
+    rk = orc.rms_norm(z, gk, EPS)
+    rrot = np.stack([[[orc.rope_rotate(rk[b, h, t], t, w, rope.amp) for t in range(T)]
+                      for h in range(Hkv)] for b in range(B)])
+    gu.compare(k_rot, rrot, what="k_rot")
+    # attention over them
+    o = torch.empty_like(qd)
+    lse = torch.empty(B, Hq, T, dtype=torch.float32, device="cuda")
+    gqa.gqa_attn_prefill(q_out, k_rot, v_out, o, lse, B, T, T, Hq, Hkv, d, window, 1.0, table,
+                         T, 1, None, 0)
+    assert gqa.gqa_get_device_status() == 0
+    qs, ks, vs = _stored(q, z, gq, gk)
+    ro, rl = orc.attention(qs, ks, vs, window=window, scale=1.0, w=w, amp=rope.amp)
+    gu.compare(o, ro, what=f"kv-shared prefill d={d} (stored bf16 tensors)")
+    gu.compare(lse, rl, what="kv-shared prefill lse")
+    ro, rl = orc.attention_kv_shared(q, z, q_gamma=gq, k_gamma=gk, eps=EPS, window=window,
+                                     scale=1.0, w=w, amp=rope.amp)
+    gu.compare(o, ro, E2E_MAX_ABS, E2E_MEAN_ABS, what=f"kv-shared prefill d={d} (end to end)")
+    gu.compare(lse, rl, E2E_MAX_ABS, E2E_MEAN_ABS, what="kv-shared prefill lse (end to end)")
+
+
+def _shared_setup(x, d):
+    """Device caches of Zn made from the raw Z caches (x.k_cache) by the norm pass, in
+    place; x.v_cache stays as a decoy the shared kernels must not read."""
+    st = DecodeSetup(x, d)
+    Hkv = x.k_new.shape[1]
+    for i, zc in enumerate(st.kc):
+        gqa.gqa_qk_norm_rope_kv_shared(None, zc, None, zc, None, 1, 0, Hkv, x.cap[i], d, 0, None,
+                                       None, EPS, None, 0)
+    assert gqa.gqa_get_device_status() == 0
+    return st
+
+
+def _shared_step(st, x, Hq, Hkv, d, gq, gk, max_len, scale=1.0):
+    nseq = x.q.shape[0]
+    q_out = torch.empty_like(st.q)
+    slots = torch.full((nseq,), -7, dtype=torch.int32, device="cuda")
+    gqa.gqa_kv_shared_append(st.descs, nseq, st.q, st.k_new, Hq, Hkv, d, _dev_gain(gq), EPS,
+                             q_out, slots)
+    o = torch.empty_like(st.q)
+    lse = torch.empty(nseq, Hq, dtype=torch.float32, device="cuda")
+    wsb = gqa.gqa_decode_workspace_bytes(nseq, Hq, d, max_len)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    gqa.gqa_attn_decode_kv_shared(q_out, st.descs, nseq, Hq, Hkv, d, scale, _dev_gain(gk),
+                                  max_len, o, lse, ws, wsb)
+    status = gqa.gqa_get_device_status()
+    assert status == 0, gqa.STATUS_NAMES.get(status, status)
+    return o, lse, slots
+
+
+def _oracle_shared(x, d, gq, gk, idx=None, scale=1.0):
+    """(end to end, stored-tensor) oracle decode steps over sequences idx: the definition
+    from the raw rows, and the plain decode over the bf16 tensors the layer stores."""
+    idx = list(range(x.q.shape[0])) if idx is None else idx
+    sub = lambda a: [a[i] for i in idx]  # noqa: E731
+    w = [gu.oracle_freq(d, r) for r in sub(x.rope)]
+    amp = [r.amp for r in sub(x.rope)]
+    args = (sub(x.cap), sub(x.count_before), sub(x.is_ring), w, amp)
+    e2e = gu.orc().decode_step_kv_shared(x.q[idx], x.k_new[idx], sub(x.k_cache), *args,
+                                         q_gamma=gq, k_gamma=gk, eps=EPS, scale=scale)
+    qs, kn, vn = _stored(x.q[idx], x.k_new[idx], gq, gk)
+    kc, vc = [], []
+    for zc in sub(x.k_cache):
+        _, k_i, v_i = _stored(x.q[:1], zc, gq, gk)
+        kc.append(k_i)
+        vc.append(v_i)
+    stored = gu.orc().decode_step(qs, kn, vn, kc, vc, *args[:3], w, amp, scale)
+    return e2e, stored
+
+
+def _check_decode(o, lse, e2e, stored, what):
+    gu.compare(o, stored[0], what=f"{what} (stored bf16 tensors)")
+    gu.compare(lse, stored[1], what=f"{what} lse (stored bf16 tensors)")
+    gu.compare(o, e2e[0], E2E_MAX_ABS, E2E_MEAN_ABS, what=f"{what} (end to end)")
+    gu.compare(lse, e2e[1], E2E_MAX_ABS, E2E_MEAN_ABS, what=f"{what} lse (end to end)")
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(16, 2, 512), (16, 8, 256), (8, 1, 128), (6, 3, 256)])
+def test_decode_kv_shared(Hq, Hkv, d):
+    """Linear caches across split boundaries and rings around wrap-around; the new token's
+    Z is normalised into its slot, the query normalised, then one decode step."""
+    gu.require_gpu()
+    x = _random_batch([0, 15, 1023, 1024, 2100], [(64, 10), (64, 200), (1024, 1023),
+                                                  (1024, 3000)], Hq, Hkv, d, seed=1700 + d + Hq)
+    x = replace(x, k_cache=[(t.float() * 3).to(torch.bfloat16) for t in x.k_cache])
+    if d == 512:
+        x = replace(x, rope=[PROPE if not r else LOCAL for r in x.is_ring])
+    gq, gk = norm_gains(d, 1800 + d), norm_gains(d, 1900 + d)
+    st = _shared_setup(x, d)
+    o, lse, slots = _shared_step(st, x, Hq, Hkv, d, gq, gk, max_len=4096)
+    e2e, stored = _oracle_shared(x, d, gq, gk)
+    _, _, rslots, rcounts = e2e
+    assert np.array_equal(slots.cpu().numpy().astype(np.int64), rslots)
+    assert np.array_equal(st.counts(), rcounts)
+    # the appended rows hold Zn of the new token; the decoy V caches are untouched
+    rz = gu.orc().rms_norm(x.k_new, None, EPS)
+    for i in range(x.q.shape[0]):
+        for h in range(Hkv):
+            gu.compare(st.kc[i][h, int(rslots[i])], rz[i, h], what=f"appended Zn {i}")
+        assert torch.equal(st.vc[i].cpu(), x.v_cache[i])
+    _check_decode(o, lse, e2e, stored, f"kv-shared decode d={d} Hq={Hq} Hkv={Hkv}")
+
+
+def test_decode_kv_shared_equals_separate_caches():
+    """The shared kernel over Zn equals the plain decode kernel over K = bf16(gamma_k) Zn
+    and V = Zn stored separately (the same bf16 keys, built here with torch): the sharing
+    changes which bytes are read, not the result."""
+    gu.require_gpu()
+    Hq, Hkv, d = 16, 2, 512
+    x = _random_batch([700, 3000], [(1024, 2500)], Hq, Hkv, d, seed=2000)
+    gk = norm_gains(d, 2001)
+    st = _shared_setup(x, d)
+    # separate caches made from the shared one
+    gk_bf = torch.from_numpy(gk).to(torch.bfloat16).cuda()
+    kc = [(zc * gk_bf).contiguous() for zc in st.kc]
+    vc = [zc.clone() for zc in st.kc]
+    a = gqa.make_kv_descs(kc, vc, [st.tables[r][0] for r in x.rope], x.cap,
+                          [c + 1 for c in x.count_before], x.is_ring,
+                          [st.tables[r][1] for r in x.rope])
+    descs_sep = torch.from_numpy(a.view(np.uint8).copy()).cuda()
+    a2 = gqa.make_kv_descs(st.kc, st.vc, [st.tables[r][0] for r in x.rope], x.cap,
+                           [c + 1 for c in x.count_before], x.is_ring,
+                           [st.tables[r][1] for r in x.rope])
+    descs_sh = torch.from_numpy(a2.view(np.uint8).copy()).cuda()
+    nseq, max_len = x.q.shape[0], 4096
+    wsb = gqa.gqa_decode_workspace_bytes(nseq, Hq, d, max_len)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    o1, o2 = torch.empty_like(st.q), torch.empty_like(st.q)
+    gqa.gqa_attn_decode(st.q, descs_sep, nseq, Hq, Hkv, d, 0.05, max_len, o1, None, ws, wsb)
+    gqa.gqa_attn_decode_kv_shared(st.q, descs_sh, nseq, Hq, Hkv, d, 0.05, _dev_gain(gk),
+                                  max_len, o2, None, ws, wsb)
+    assert gqa.gqa_get_device_status() == 0
+    assert torch.equal(o1, o2)
+
+
+def test_gemma4_decode_global_kv_shared_full_size_sampled():
+    """The benchmark's batch: 32 global caches of 8192..65536 tokens, d = 512, 2 KV heads,
+    p-RoPE, one launch over every sequence; 6 sequences (the longest, the shortest and 4
+    seeded others) compared with the oracle, all slots and counts bit-exact."""
+    gu.require_gpu()
+    w = get_workload("gemma4_decode_global_kv_shared")
+    x = decode_inputs(w)
+    gq, gk = norm_gains(w.d, w.seed + 1), norm_gains(w.d, w.seed + 2)
+    st = _shared_setup(x, w.d)
+    max_len = max(w.global_len_range[1], w.window)
+    o, lse, slots = _shared_step(st, x, w.Hq, w.Hkv, w.d, gq, gk, max_len, w.scale)
+    lens = np.array(x.count_before)
+    rng = np.random.default_rng(11)
+    idx = sorted({int(lens.argmax()), int(lens.argmin())} |
+                 set(rng.choice(w.nseq, 4, replace=False).tolist()))
+    e2e, stored = _oracle_shared(x, w.d, gq, gk, idx, w.scale)
+    rslots = e2e[2]
+    want_slots = [gu.orc().append_slot(r, c, cap)
+                  for r, c, cap in zip(x.is_ring, x.count_before, x.cap)]
+    assert slots.cpu().tolist() == want_slots
+    assert st.counts().tolist() == [c + 1 for c in x.count_before]
+    assert rslots.tolist() == [want_slots[i] for i in idx]
+    _check_decode(o[idx], lse[idx], e2e, stored, "gemma4 kv-shared decode (sampled sequences)")

@@ -31,4 +31,5 @@ from .gen import (  # noqa: F401
     prefill_inputs,
     decode_inputs,
     bf16_bits,
+    norm_gains,
 )

@@ -74,6 +74,9 @@ class DecodeWorkload:
     rope_local: RopeSpec
     scale: float
     seed: int
+    # K and V from one shared projection (Gemma 4 global layers, attention_k_eq_v): the
+    # caches hold Zn = N_1(Z) only; keys RoPE(gamma_k Zn), values Zn
+    kv_shared: bool = False
 
     @property
     def nseq(self) -> int:
@@ -121,6 +124,13 @@ GEMMA4_DECODE_GLOBAL = DecodeWorkload(
     "gemma4_decode_global", n_global=32, n_local=0, Hq=16, Hkv=2, d=512,
     global_len_range=(8192, 65536), window=1024, rope_global=_G4_GLOBAL,
     rope_local=_G4_LOCAL, scale=1 / math.sqrt(512), seed=6006)
+# The global layer as Gemma 4 defines it (attention_k_eq_v, "PLaMo 3アーキテクチャ徹底解析"
+# §5.2 and §8): one cache of Zn per sequence for both K and V, scale 1 with the gains
+# carrying the logit scale; the same lengths as gemma4_decode_global (same seed).
+GEMMA4_DECODE_GLOBAL_KV_SHARED = DecodeWorkload(
+    "gemma4_decode_global_kv_shared", n_global=32, n_local=0, Hq=16, Hkv=2, d=512,
+    global_len_range=(8192, 65536), window=1024, rope_global=_G4_GLOBAL,
+    rope_local=_G4_LOCAL, scale=1.0, seed=6006, kv_shared=True)
 GEMMA4_DECODE_LOCAL = DecodeWorkload(
     "gemma4_decode_local", n_global=0, n_local=32, Hq=16, Hkv=8, d=256,
     global_len_range=(1024, 1024), window=1024, rope_global=_G4_GLOBAL,
@@ -154,7 +164,8 @@ PLAMO3_DECODE_64LAYER = DecodeModelWorkload(
 
 WORKLOADS = {w.name: w for w in (TINY_W64, TINY_CAUSAL, PLAMO3_LOCAL_PREFILL,
                                  PLAMO3_GLOBAL_PREFILL, PLAMO3_DECODE, GEMMA4_PERIOD,
-                                 GEMMA4_DECODE_GLOBAL, GEMMA4_DECODE_LOCAL,
+                                 GEMMA4_DECODE_GLOBAL, GEMMA4_DECODE_GLOBAL_KV_SHARED,
+                                 GEMMA4_DECODE_LOCAL,
                                  PLAMO3_DECODE_64LAYER)}
 
 

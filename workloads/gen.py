@@ -5,6 +5,7 @@ x86 and on Arm hosts.  Tensors are returned on the CPU; callers move them.
 """
 from __future__ import annotations
 
+import math
 from dataclasses import dataclass
 from typing import List
 
@@ -94,3 +95,13 @@ def decode_inputs(w: DecodeWorkload, cap_slack: int = 0) -> DecodeInputs:
         k_cache.append(randn_bf16((w.Hkv, c, w.d), base + 100 + 2 * i))
         v_cache.append(randn_bf16((w.Hkv, c, w.d), base + 101 + 2 * i))
     return DecodeInputs(q, k_new, v_new, k_cache, v_cache, cap, count, ring, rope)
+
+
+def norm_gains(d: int, seed: int) -> np.ndarray:
+    """A per-layer RMSNorm gain [d] for a layer with attention scale 1 (Gemma 4): values
+    around d^(-1/4) with 20% spread, so a query/key gain pair gives logits of standard
+    deviation ~1 on unit-RMS rows (what scale 1/sqrt(d) gives the other workloads).
+    Rounded to bf16 values (as stored weights are), returned as float64."""
+    g = torch.randn(d, generator=_gen(seed), dtype=torch.float32)
+    level = d ** -0.25
+    return (level * (1.0 + 0.2 * g)).to(torch.bfloat16).to(torch.float64).numpy()
