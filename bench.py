@@ -77,9 +77,7 @@ def traffic_record(kernel: str, workload: str):
 
 def kernel_name(L) -> str:
     from global_causal_gqa_gb300 import accounting as acc
-    if L.d == 128:
-        return acc.prefill_d128_kernel(L.T, L.S, L.window)
-    return f"prefill_wide_kernel<{L.d}>"
+    return acc.prefill_kernel_name(L.d, L.T, L.S, L.window)
 
 
 class ClockSampler:
@@ -340,7 +338,7 @@ def e2e_prefill(L, st, steps, warmup, stream, flops):
     ms = statistics.mean(a for (a,) in timer.durations_ms())
     nb = lambda t: t.numel() * t.element_size()  # noqa: E731
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": sum(nb(h) for h, _ in ins), "d2h_bytes_per_step": nb(oh)}
+            "h2d_bytes_per_step": nb(qh) + nb(kh) + nb(vh), "d2h_bytes_per_step": nb(oh)}
 
 
 # ----------------------------------------------------------------------------------------
