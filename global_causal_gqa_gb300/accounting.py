@@ -60,11 +60,9 @@ def kv_capacity_bytes(layers, N: int, elem_bytes: int = 2) -> int:
     return total
 
 
-def prefill_d128_kernel(T: int, S: int, window: int) -> str:
-    """Which d = 128 prefill kernel the library launches for these positions: the
-    one-CTA-per-item kernel when the 128-row query blocks average at least 48 key tiles
-    (long causal sweeps), the persistent kernel otherwise.  Mirrors the rule in the
-    library's launcher; used to label measurements."""
+def _short_items(T: int, S: int, window: int) -> bool:
+    """Whether the 128-row query blocks average fewer than 48 key tiles (windowed layers,
+    short sequences): the library's launchers then pick their persistent kernels."""
     n_mb = -(-T // 128)
     tiles = 0
     for mb in range(n_mb):
@@ -72,4 +70,19 @@ def prefill_d128_kernel(T: int, S: int, window: int) -> str:
         q_hi = min(q_lo + 127, S - 1)
         kt0 = max(0, q_lo - window + 1) // 128 if window > 0 else 0
         tiles += q_hi // 128 - kt0 + 1
-    return "prefill_kernel" if tiles >= 48 * n_mb else "prefill_persistent_kernel"
+    return tiles < 48 * n_mb
+
+
+def prefill_d128_kernel(T: int, S: int, window: int) -> str:
+    """Which d = 128 prefill kernel the library launches for these positions: the
+    one-CTA-per-item kernel when the 128-row query blocks average at least 48 key tiles
+    (long causal sweeps), the persistent kernel otherwise.  Mirrors the rule in the
+    library's launcher; used to label measurements."""
+    return "prefill_persistent_kernel" if _short_items(T, S, window) else "prefill_kernel"
+
+
+def prefill_kernel_name(d: int, T: int, S: int, window: int) -> str:
+    """The prefill kernel the library launches for head dim d at these positions."""
+    if d == 128:
+        return prefill_d128_kernel(T, S, window)
+    return f"prefill_wide_kernel<{d}>"

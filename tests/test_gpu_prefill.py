@@ -184,3 +184,19 @@ def test_stream_kernel_medium_causal_sampled():
     from global_causal_gqa_gb300 import accounting as acc
     assert acc.prefill_d128_kernel(layer.T, layer.S, layer.window) == "prefill_kernel"
     _sampled_case(layer, 2048, 7)
+
+
+def test_wide_many_items_sampled():
+    """d = 256 windowed layer with far more query blocks than SMs, a history before the
+    queries, ragged windows and single-tile query blocks."""
+    _sampled_case(_layer(2, 4000, 4100, 8, 4, 384, d=256, seed=83), 2048, 8)
+
+
+def test_wide_single_tile_items():
+    """Every query block a single key tile (window 1 at d = 256)."""
+    _full_case(_layer(1, 1100, 1100, 4, 2, 1, d=256, seed=84))
+
+
+def test_wide_long_causal_sampled():
+    """d = 256 causal sweep over 97 query blocks of up to 97 key tiles each."""
+    _sampled_case(_layer(1, 12400, 12400, 2, 1, 0, d=256, seed=85), 1024, 9)
