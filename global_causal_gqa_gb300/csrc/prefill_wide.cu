@@ -279,45 +279,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qpos = p.S - p.T + t;
         bool ok = warp_wait_w(&bars->q_full, 0);
         if (!ok) set_timeout(p.status, kDiagPrefillWide, 3, 8, 0);
-        if (ok && valid) {
-            // RoPE on the Q row: pair (j, j + D/2) = same swizzled offset in boxes k, k + D/128
-            const float2 *tab = p.table + (size_t)qpos * (D / 2);
-            for (int kc = 0; kc < 2 * (D / 128); ++kc) {
-                const int kb = kc >> 1;
-                uint8_t *row0 = sQ + kb * QBOX + r * 128;
-                uint8_t *row1 = row0 + (D / 128) * QBOX;
-                // the table entries of four chunks in flight at once
-                float4 tv4[16];
-                const float4 *t4 = reinterpret_cast<const float4 *>(tab + 64 * kb + 32 * (kc & 1));
+        if (ok) {
+            // RoPE on the Q tile, one row at a time per warp (warp w4 takes rows 32 w4 ..
+            // 32 w4 + 31): lane l rotates pairs 64 b + 2l, 64 b + 2l + 1 of every 64-pair
+            // box b against their partners D/2 later (the same swizzled word of box b + NB).
+            // The table row is read as NB coalesced 512-byte pieces, RIF rows in flight.
+            constexpr int NB = D / 128;           // 64-pair boxes in each half of a row
+            constexpr int RIF = 32 / NB;          // rows whose table loads are in flight
+            const int w4 = warp & 3;
+            const float4 *t4 = reinterpret_cast<const float4 *>(p.table);
+            for (int r0 = 0; r0 < 32; r0 += RIF) {
+                float4 tv[RIF][NB];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) tv4[i] = __ldg(t4 + i);
+                for (int i = 0; i < RIF; ++i) {
+                    const int row = 32 * w4 + r0 + i;
+                    // rows past T hold zeros (the load's out-of-range fill): any table row
+                    const int pos = min(p.S - p.T + mb * kBM + row, p.S - 1);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c = 4 * (kc & 1) + cc;
-                    const int pc = (c ^ (r & 7)) * 16;
-                    uint4 a = *reinterpret_cast<uint4 *>(row0 + pc);
-                    uint4 bq = *reinterpret_cast<uint4 *>(row1 + pc);
-                    float cs[16];
+                    for (int bb = 0; bb < NB; ++bb)
+                        tv[i][bb] = __ldg(t4 + (size_t)pos * (D / 4) + 32 * bb + lane);
+                }
 #pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) {
-                        const float4 tv = tv4[4 * cc + qq];
-                        cs[4 * qq] = tv.x;
-                        cs[4 * qq + 1] = tv.y;
-                        cs[4 * qq + 2] = tv.z;
-                        cs[4 * qq + 3] = tv.w;
+                for (int i = 0; i < RIF; ++i) {
+                    const int row = 32 * w4 + r0 + i;
+                    const int off = row * 128 + ((((lane >> 2) ^ (row & 7)) << 4) | ((lane & 3) << 2));
+#pragma unroll
+                    for (int bb = 0; bb < NB; ++bb) {
+                        uint32_t *pa = reinterpret_cast<uint32_t *>(sQ + bb * QBOX + off);
+                        uint32_t *pb = reinterpret_cast<uint32_t *>(sQ + (bb + NB) * QBOX + off);
+                        const float4 t = tv[i][bb];   // (cos, sin) of the two pairs
+                        const uint32_t aw = *pa, bw = *pb;
+                        const float a0 = bf16lo(aw), a1 = bf16hi(aw);
+                        const float b0 = bf16lo(bw), b1 = bf16hi(bw);
+                        *pa = pack_bf16x2(fmaf(a0, t.x, -b0 * t.y), fmaf(a1, t.z, -b1 * t.w));
+                        *pb = pack_bf16x2(fmaf(a0, t.y, b0 * t.x), fmaf(a1, t.w, b1 * t.z));
                     }
-                    uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) {
-                        const float a0 = bf16lo(aw[qq]), a1 = bf16hi(aw[qq]);
-                        const float b0 = bf16lo(bw[qq]), b1 = bf16hi(bw[qq]);
-                        const float c0 = cs[4 * qq], s0 = cs[4 * qq + 1];
-                        const float c1 = cs[4 * qq + 2], s1 = cs[4 * qq + 3];
-                        aw[qq] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
-                        bw[qq] = pack_bf16x2(fmaf(a0, s0, b0 * c0), fmaf(a1, s1, b1 * c1));
-                    }
-                    *reinterpret_cast<uint4 *>(row0 + pc) = make_uint4(aw[0], aw[1], aw[2], aw[3]);
-                    *reinterpret_cast<uint4 *>(row1 + pc) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
                 }
             }
         }
@@ -450,7 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_store_3d(&tmO, sQ + bx * QBOX, slice * DV + 64 * bx, mb * kBM,
                                      b * p.Hq + h);
                     bulk_commit_group();
-                    bulk_wait_all();   // complete before the CTA (and its shared memory) ends
+                    // the stores have read the staging area before the CTA (and its
+                    // shared memory) ends; their writes complete on their own
+                    bulk_wait_read_all();
                 }
             }
             if (valid && p.lse && slice == 0)
