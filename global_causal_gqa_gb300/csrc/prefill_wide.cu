@@ -18,8 +18,9 @@
 //            (the score contraction runs over all 512 dims) and each accumulates half of
 //            O; Q 128 KB + 3 ring slots.
 // Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2-3 idle, 4-7 softmax/epilogue (one
-// thread per query row).  Q is rotated (RoPE) in shared memory after it lands; pairs
-// (j, j + d/2) sit at the same offset of boxes k and k + d/128.
+// thread per query row).  Q is rotated (RoPE) in shared memory after it lands, by all 8
+// warps, while the first K tiles load; pairs (j, j + d/2) sit at the same offset of boxes
+// k and k + d/128.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
-        mbar_init(&bars->q_ready, 128);
+        mbar_init(&bars->q_ready, kThreads);
         for (int i = 0; i < NS; ++i) {
             mbar_init(&bars->full[i], 1);
             mbar_init(&bars->empty[i], 1);
@@ -142,48 +143,122 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // The ring sequence, shared by the producer and the MMA thread: K(0), K(1), then for
     // j = 0 .. n-1: V(j), and K(j + 2) if it exists; each K is NKC slots, each V is NVH.
-    if (warp == 0) {
-        // ================= TMA producer: Q, then the ring =================
-        if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            const int zq = b * p.Hq + h, zk = b * p.Hkv + g;
-            mbar_arrive_expect_tx(&bars->q_full, QBYTES);
-            for (int i = 0; i < D / 64; ++i)
-                tma_load_3d(sQ + i * QBOX, &tmQ, &bars->q_full, 64 * i, mb * kBM, zq);
-            bool ok = true;
-            int u = 0;
-            // one 32 KB slot: rows n0 .. n0 + 127, columns c0 .. c0 + 127 of K or V
-            auto put = [&](const CUtensorMap *map, int n0, int c0) {
-                const int st = u % NS;
-                if (u >= NS && !(ok = mbar_wait(&bars->empty[st], ((u / NS) - 1) & 1))) {
-                    set_timeout(p.status, kDiagPrefillWide, 0, 1, u);
-                    return;
+    // Slot load u of the sequence: its tensor, its key tile and its 128 columns.
+    const int n_k0 = NKC * min(2, n_tiles);      // the loads of K(0), K(1)
+    const int n_pair = max(0, n_tiles - 2);      // tiles j with a K(j + 2) after V(j)
+    const int n_loads = (NKC + NVH) * n_tiles;
+    auto slot_load = [&](int u, const CUtensorMap *&map, int &jt, int &c0) {
+        if (u < n_k0) {
+            map = &tmK;
+            jt = u / NKC;
+            c0 = 128 * (u % NKC);
+            return;
+        }
+        int v = u - n_k0, j, w;
+        if (v < n_pair * (NKC + NVH)) {
+            j = v / (NKC + NVH);
+            w = v % (NKC + NVH);
+        } else {
+            v -= n_pair * (NKC + NVH);
+            j = n_pair + v / NVH;
+            w = v % NVH;
+        }
+        if (w < NVH) {
+            map = &tmV;
+            jt = j;
+            c0 = slice * DV + 128 * w;
+        } else {
+            map = &tmK;
+            jt = j + 2;
+            c0 = 128 * (w - NVH);
+        }
+    };
+    // producer state (warp 0, lane 0)
+    int pu = 0;
+    bool pok = true;
+    // one 32 KB slot: rows of key tile jt, columns c0 .. c0 + 127 of K or V
+    auto put = [&]() {
+        const int st = pu % NS;
+        if (pu >= NS && !(pok = mbar_wait(&bars->empty[st], ((pu / NS) - 1) & 1))) {
+            set_timeout(p.status, kDiagPrefillWide, 0, 1, pu);
+            return;
+        }
+        const CUtensorMap *map;
+        int jt, c0;
+        slot_load(pu, map, jt, c0);
+        const int n0 = (kt_first + jt) * BN, zk = b * p.Hkv + g;
+        uint8_t *dst = smem + OFF_RING + st * kSlotBytes;
+        mbar_arrive_expect_tx(&bars->full[st], kSlotBytes);
+        tma_load_3d(dst, map, &bars->full[st], c0, n0, zk);
+        tma_load_3d(dst + BOX, map, &bars->full[st], c0 + 64, n0, zk);
+        ++pu;
+    };
+    if (warp == 0 && lane == 0) {
+        // Q, then the ring loads that need no free slot, before the rotation below
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        mbar_arrive_expect_tx(&bars->q_full, QBYTES);
+        for (int i = 0; i < D / 64; ++i)
+            tma_load_3d(sQ + i * QBOX, &tmQ, &bars->q_full, 64 * i, mb * kBM, b * p.Hq + h);
+        while (pu < min(NS, n_loads)) put();
+    }
+
+    // ================= RoPE on the Q tile, by every warp =================
+    // Warp w takes rows QR w .. QR w + QR - 1, one row at a time: lane l rotates pairs
+    // 64 bb + 2l, 64 bb + 2l + 1 of every 64-pair box bb against their partners D/2 later
+    // (the same swizzled word of box bb + NB).  The table row is read as NB coalesced
+    // 512-byte pieces, RIF rows in flight.
+    {
+        constexpr int NB = D / 128;               // 64-pair boxes in each half of a row
+        constexpr int QR = kBM / (kThreads / 32);   // rows per warp
+        constexpr int RIF = QR < 32 / NB ? QR : 32 / NB;   // rows whose table loads are in flight
+        bool qok = warp_wait_w(&bars->q_full, 0);
+        if (!qok) set_timeout(p.status, kDiagPrefillWide, 3, 8, 0);
+        if (qok) {
+            const float4 *t4 = reinterpret_cast<const float4 *>(p.table);
+            for (int r0 = 0; r0 < QR; r0 += RIF) {
+                float4 tv[RIF][NB];
+#pragma unroll
+                for (int i = 0; i < RIF; ++i) {
+                    const int row = QR * warp + r0 + i;
+                    // rows past T hold zeros (the load's out-of-range fill): any table row
+                    const int pos = min(p.S - p.T + mb * kBM + row, p.S - 1);
+#pragma unroll
+                    for (int bb = 0; bb < NB; ++bb)
+                        tv[i][bb] = __ldg(t4 + (size_t)pos * (D / 4) + 32 * bb + lane);
                 }
-                uint8_t *dst = smem + OFF_RING + st * kSlotBytes;
-                mbar_arrive_expect_tx(&bars->full[st], kSlotBytes);
-                tma_load_3d(dst, map, &bars->full[st], c0, n0, zk);
-                tma_load_3d(dst + BOX, map, &bars->full[st], c0 + 64, n0, zk);
-                ++u;
-            };
-            auto put_k = [&](int j) {
-                for (int c = 0; c < NKC && ok; ++c) put(&tmK, (kt_first + j) * BN, 128 * c);
-            };
-            auto put_v = [&](int j) {
-                for (int hh = 0; hh < NVH && ok; ++hh)
-                    put(&tmV, (kt_first + j) * BN, slice * DV + 128 * hh);
-            };
-            put_k(0);
-            if (n_tiles > 1) put_k(1);
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                put_v(j);
-                if (j + 2 < n_tiles) put_k(j + 2);
+#pragma unroll
+                for (int i = 0; i < RIF; ++i) {
+                    const int row = QR * warp + r0 + i;
+                    const int off =
+                        row * 128 + ((((lane >> 2) ^ (row & 7)) << 4) | ((lane & 3) << 2));
+#pragma unroll
+                    for (int bb = 0; bb < NB; ++bb) {
+                        uint32_t *pa = reinterpret_cast<uint32_t *>(sQ + bb * QBOX + off);
+                        uint32_t *pb = reinterpret_cast<uint32_t *>(sQ + (bb + NB) * QBOX + off);
+                        const float4 t = tv[i][bb];   // (cos, sin) of the two pairs
+                        const uint32_t aw = *pa, bw = *pb;
+                        const float a0 = bf16lo(aw), a1 = bf16hi(aw);
+                        const float b0 = bf16lo(bw), b1 = bf16hi(bw);
+                        *pa = pack_bf16x2(fmaf(a0, t.x, -b0 * t.y), fmaf(a1, t.z, -b1 * t.w));
+                        *pb = pack_bf16x2(fmaf(a0, t.y, b0 * t.x), fmaf(a1, t.w, b1 * t.z));
+                    }
+                }
             }
-            if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->q_ready);
+    }
+
+    if (warp == 0) {
+        // ================= TMA producer: the rest of the ring =================
+        if (lane == 0) {
+            while (pok && pu < n_loads) put();
+            if (!pok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
             // never leave the CTA with copies in flight
             mbar_wait(&bars->q_full, 0);
-            for (int w = max(0, u - NS); w < u; ++w) mbar_wait(&bars->full[w % NS], (w / NS) & 1);
+            for (int w = max(0, pu - NS); w < pu; ++w) mbar_wait(&bars->full[w % NS], (w / NS) & 1);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -277,48 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = mb * kBM + r;
         const bool valid = t < p.T;
         const int qpos = p.S - p.T + t;
-        bool ok = warp_wait_w(&bars->q_full, 0);
-        if (!ok) set_timeout(p.status, kDiagPrefillWide, 3, 8, 0);
-        if (ok) {
-            // RoPE on the Q tile, one row at a time per warp (warp w4 takes rows 32 w4 ..
-            // 32 w4 + 31): lane l rotates pairs 64 b + 2l, 64 b + 2l + 1 of every 64-pair
-            // box b against their partners D/2 later (the same swizzled word of box b + NB).
-            // The table row is read as NB coalesced 512-byte pieces, RIF rows in flight.
-            constexpr int NB = D / 128;           // 64-pair boxes in each half of a row
-            constexpr int RIF = 32 / NB;          // rows whose table loads are in flight
-            const int w4 = warp & 3;
-            const float4 *t4 = reinterpret_cast<const float4 *>(p.table);
-            for (int r0 = 0; r0 < 32; r0 += RIF) {
-                float4 tv[RIF][NB];
-#pragma unroll
-                for (int i = 0; i < RIF; ++i) {
-                    const int row = 32 * w4 + r0 + i;
-                    // rows past T hold zeros (the load's out-of-range fill): any table row
-                    const int pos = min(p.S - p.T + mb * kBM + row, p.S - 1);
-#pragma unroll
-                    for (int bb = 0; bb < NB; ++bb)
-                        tv[i][bb] = __ldg(t4 + (size_t)pos * (D / 4) + 32 * bb + lane);
-                }
-#pragma unroll
-                for (int i = 0; i < RIF; ++i) {
-                    const int row = 32 * w4 + r0 + i;
-                    const int off = row * 128 + ((((lane >> 2) ^ (row & 7)) << 4) | ((lane & 3) << 2));
-#pragma unroll
-                    for (int bb = 0; bb < NB; ++bb) {
-                        uint32_t *pa = reinterpret_cast<uint32_t *>(sQ + bb * QBOX + off);
-                        uint32_t *pb = reinterpret_cast<uint32_t *>(sQ + (bb + NB) * QBOX + off);
-                        const float4 t = tv[i][bb];   // (cos, sin) of the two pairs
-                        const uint32_t aw = *pa, bw = *pb;
-                        const float a0 = bf16lo(aw), a1 = bf16hi(aw);
-                        const float b0 = bf16lo(bw), b1 = bf16hi(bw);
-                        *pa = pack_bf16x2(fmaf(a0, t.x, -b0 * t.y), fmaf(a1, t.z, -b1 * t.w));
-                        *pb = pack_bf16x2(fmaf(a0, t.y, b0 * t.x), fmaf(a1, t.w, b1 * t.z));
-                    }
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars->q_ready);
+        bool ok = true;
 
         float m = -CUDART_INF_F, l = 0.f;
         for (int j = 0; j < n_tiles && ok; ++j) {
