@@ -199,11 +199,14 @@ def barrier(world):
 
 
 def max_over_ranks(world, value: float) -> float:
+    """The largest of the ranks' values (the step time every rank reports is the slowest
+    rank's); NCCL reduces a device tensor, gloo (CPU runs) a host one."""
     if world == 1:
         return value
     import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
