@@ -243,7 +243,7 @@ gqa_status gqa_kv_shared_append(gqa_kv_desc *descs, int nseq, const void *q, con
  * R > max_len or rope_len < R is skipped and flagged in the status word.
  * workspace: device scratch of gqa_decode_workspace_bytes(nseq, Hq, d, max_len) bytes:
  * nseq Hq nsplit (d + 2) floats of split partials, nsplit = ceil(max_len / chunk) with
- * chunk = 1024 keys when max_len > 4096 and 256 otherwise.
+ * chunk = 2048 keys when max_len > 4096 and 256 otherwise.
  * d in {128, 256, 512} (Gemma-4 local / global heads), Hq/Hkv <= 8. */
 size_t gqa_decode_workspace_bytes(int nseq, int Hq, int d, int max_len);
 gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq,

@@ -41,10 +41,10 @@ def test_yarn_amplitude_and_sizes():
     assert abs(gqa.gqa_yarn_amplitude(256.0) - (1 + 0.1 * math.log(256))) < 1e-15
     assert gqa.gqa_rope_table_bytes(128, 1000) == 1000 * 64 * 2 * 4
     assert gqa.gqa_prefill_workspace_bytes(2, 8, 8192, 128) == 2 * 8 * 8192 * 128 * 2
-    assert gqa.gqa_decode_workspace_bytes(32, 64, 128, 65536) == 32 * 64 * 64 * 130 * 4
+    assert gqa.gqa_decode_workspace_bytes(32, 64, 128, 65536) == 32 * 64 * 32 * 130 * 4  # 2048-key splits
     # short caches split every 256 keys
     assert gqa.gqa_decode_workspace_bytes(32, 16, 256, 1024) == 32 * 16 * 4 * 258 * 4
-    assert gqa.gqa_decode_workspace_bytes(2, 8, 512, 4097) == 2 * 8 * 5 * 514 * 4
+    assert gqa.gqa_decode_workspace_bytes(2, 8, 512, 4097) == 2 * 8 * 3 * 514 * 4
     assert gqa.gqa_rope_table_bytes(0, 10) == 0
 
 
