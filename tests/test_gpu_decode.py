@@ -190,3 +190,21 @@ def test_wide_head_decode(Hq, Hkv, d):
     assert np.array_equal(st.counts(), rcounts)
     gu.compare(o, ro, what=f"decode d={d} Hq={Hq} Hkv={Hkv}")
     gu.compare(lse, rl, what="decode lse")
+
+
+def test_long_split_boundaries():
+    """max_len > 4096 (2048-key splits): caches ending just before, at and after split
+    boundaries, a split that holds a single key, and rings that wrap."""
+    gu.require_gpu()
+    Hq, Hkv = 16, 2
+    lengths = [2047, 2048, 2049, 4095, 4096, 4097, 6143]
+    rings = [(2048, 2047), (2048, 5000)]
+    x = _random_batch(lengths, rings, Hq, Hkv, seed=77)
+    st = DecodeSetup(x, 128)
+    scale = 1 / math.sqrt(128)
+    o, lse, slots = run_step(st, Hq, Hkv, scale, max_len=8192)
+    ro, rl, rslots, rcounts = oracle_step(x, 128, scale)
+    assert np.array_equal(slots.cpu().numpy().astype(np.int64), rslots)
+    assert np.array_equal(st.counts(), rcounts)
+    gu.compare(o, ro, what="decode, 2048-key splits")
+    gu.compare(lse, rl, what="decode lse, 2048-key splits")

@@ -185,6 +185,22 @@ def test_decode_kv_shared(Hq, Hkv, d):
     _check_decode(o, lse, e2e, stored, f"kv-shared decode d={d} Hq={Hq} Hkv={Hkv}")
 
 
+def test_decode_kv_shared_long_splits():
+    """max_len > 4096 (2048-key splits) with split-boundary lengths, d = 512."""
+    gu.require_gpu()
+    Hq, Hkv, d = 16, 2, 512
+    x = _random_batch([2047, 2048, 2049, 4100], [(1024, 3000)], Hq, Hkv, d, seed=2100)
+    x = replace(x, k_cache=[(t.float() * 3).to(torch.bfloat16) for t in x.k_cache],
+                rope=[PROPE if not r else LOCAL for r in x.is_ring])
+    gq, gk = norm_gains(d, 2101), norm_gains(d, 2102)
+    st = _shared_setup(x, d)
+    o, lse, slots = _shared_step(st, x, Hq, Hkv, d, gq, gk, max_len=8192)
+    e2e, stored = _oracle_shared(x, d, gq, gk)
+    assert np.array_equal(slots.cpu().numpy().astype(np.int64), e2e[2])
+    assert np.array_equal(st.counts(), e2e[3])
+    _check_decode(o, lse, e2e, stored, "kv-shared decode, 2048-key splits")
+
+
 def test_decode_kv_shared_equals_separate_caches():
     """The shared kernel over Zn equals the plain decode kernel over K = bf16(gamma_k) Zn
     and V = Zn stored separately (the same bf16 keys, built here with torch): the sharing
