@@ -709,7 +709,7 @@ def run_reference(args, wl, world, rank):
     is_decode = isinstance(wl, DecodeWorkload)
     target = wl if is_decode else wl.layers[0]
     per_step = float(os.environ.get("GQA_REF_STEP_SECONDS", "3"))
-    vals = []
+    vals, secs = [], []
     for i in range(args.warmup + args.steps):
         if is_decode:
             v, info = oracle_decode_sample(target, per_step, seed=i)
@@ -717,15 +717,16 @@ def run_reference(args, wl, world, rank):
             v, info = oracle_prefill_sample(target, per_step, seed=i)
         if i >= args.warmup:
             vals.append(v)
+            secs.append(info["seconds"])
     value = statistics.mean(vals)
     unit = "GB/s" if is_decode else "TFLOP/s"
     sample = (f"each step: {info.get('sequences', info.get('rows'))} "
               f"{'sequences' if is_decode else 'random query rows'} of {wl.name}, fp64")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(wl),
+            "ms_per_step": 1e3 * statistics.mean(secs), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {**config_of(wl), "parallelism": f"host cores x{os.cpu_count()}"},
             "cpu_baseline": {"value": value, "unit": unit, "cores": os.cpu_count(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
