@@ -25,8 +25,9 @@
 // Shared K/V projection (Gemma 4 global layers, attention_k_eq_v, §5.2 and §8 of the same
 // page): the cache holds one row Zn = N_1(Z) per token; the values are Zn and the keys
 // RoPE(bf16(gamma_k) * Zn), the gain applied in bf16 to each loaded K fragment before the
-// rotation.  The V fragments are loaded from the same rows, so HBM delivers each row once
-// (the second read of a line is served by L2): half the bytes of separate K and V.
+// rotation.  Each row is loaded once, in the K layout; the V fragments are the 8x8
+// transposes (movmatrix) of those registers taken before the gain and the rotation, so
+// every byte of the cache crosses L1 once: half the traffic of separate K and V.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -253,12 +254,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             bl.k0[c] = ld_stream(kr0 + gchunk(4 * c + tq));
             bl.k1[c] = ld_stream(kr1 + gchunk(4 * c + tq));
         }
+        if constexpr (!SHARED) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int key = min(kb + 2 * tq + (i & 1) + ((i >> 1) << 3), k_end - 1);
-            const uint4 *vr = reinterpret_cast<const uint4 *>(vbase + (size_t)slot_of(key) * d);
-            bl.vv[i][0] = ld_stream(vr + gchunk(gq));
-            bl.vv[i][1] = ld_stream(vr + gchunk(8 + gq));
+            for (int i = 0; i < 4; ++i) {
+                const int key = min(kb + 2 * tq + (i & 1) + ((i >> 1) << 3), k_end - 1);
+                const uint4 *vr =
+                    reinterpret_cast<const uint4 *>(vbase + (size_t)slot_of(key) * d);
+                bl.vv[i][0] = ld_stream(vr + gchunk(gq));
+                bl.vv[i][1] = ld_stream(vr + gchunk(8 + gq));
+            }
         }
         // table rows kb .. kb + 15: instruction i copies row i (clamped), lane = 16-byte
         // piece of the row, i.e. pairs 2 lane, 2 lane + 1 = 32c + 8tq + 2qq
@@ -286,7 +290,20 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         else cp_async_wait<0>();
         __syncwarp();
         const float4 *stg = stage_base + (((kb - k_start) >> 4) & 1) * 512;
+        // Shared rows: the V^T fragments are the transposes of the raw K-layout words.
+        // Word q of chunk c of key row kb + gq (k0; kb + gq + 8 for k1) is element
+        // 8 gchunk(4c + tq) + 2q + {0, 1}; seen as an 8x8 matrix (row = key gq, column =
+        // 2tq + j), its transpose gives this thread keys 2tq, 2tq + 1 (+8 for k1) of dim
+        // 8 gchunk(4c + (gq >> 1)) + 2q + (gq & 1).
+        uint32_t vt0[4][4], vt1[4][4];
         if constexpr (SHARED) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    vt0[c][qq] = transpose8x8(word(bl.k0[c], qq));
+                    vt1[c][qq] = transpose8x8(word(bl.k1[c], qq));
+                }
             // keys = bf16(gamma_k) * Zn before the rotation; chunk lc holds elements
             // 8 gchunk(lc) .. + 7 in order, as does word group gchunk(lc) of the gain
 #pragma unroll
@@ -355,18 +372,28 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         m_run1 = mn1;
         const uint32_t pb0 = transpose8x8(pack_bf16x2(p0, p1));
         const uint32_t pb1 = transpose8x8(pack_bf16x2(p2, p3));
-        // O^T (128 dims x 8 heads) += V^T P^T; dims permuted: row g of m-tile mt is
-        // dim 64 (mt >> 2) + 8g + 2 (mt & 3), row g + 8 is the dim after it.
+        // O^T (128 dims x 8 heads) += V^T P^T; dims permuted.  Separate V: row g of m-tile
+        // mt is dim 64 (mt >> 2) + 8g + 2 (mt & 3), row g + 8 the dim after it.  Shared
+        // rows: m-tile mt = 2c + (q >> 1) takes words q (rows 0..7) and q + 1 (rows 8..15)
+        // of chunk c, q even.
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
             o[mt][0] *= f0;
             o[mt][1] *= f1;
             o[mt][2] *= f0;
             o[mt][3] *= f1;
-            const uint32_t w0 = word(bl.vv[0][mt >> 2], mt & 3), w1 = word(bl.vv[1][mt >> 2], mt & 3);
-            const uint32_t w2 = word(bl.vv[2][mt >> 2], mt & 3), w3 = word(bl.vv[3][mt >> 2], mt & 3);
-            mma16816(o[mt], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
-                     __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), pb0, pb1);
+            if constexpr (SHARED) {
+                const int c = mt >> 1, qq = 2 * (mt & 1);
+                mma16816(o[mt], vt0[c][qq], vt0[c][qq + 1], vt1[c][qq], vt1[c][qq + 1], pb0,
+                         pb1);
+            } else {
+                const uint32_t w0 = word(bl.vv[0][mt >> 2], mt & 3);
+                const uint32_t w1 = word(bl.vv[1][mt >> 2], mt & 3);
+                const uint32_t w2 = word(bl.vv[2][mt >> 2], mt & 3);
+                const uint32_t w3 = word(bl.vv[3][mt >> 2], mt & 3);
+                mma16816(o[mt], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
+                         __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), pb0, pb1);
+            }
         }
     };
 
@@ -396,6 +423,47 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     auto out_off = [&](int i) {
         return (i >> 1) * (d / 2) + 64 * part + 8 * gq + 4 * (i & 1);
     };
+    if constexpr (SHARED) {
+        // This thread holds, for chunk c, dims b + 2q + par (q = 0..3, par = gq & 1,
+        // b = 8 gchunk(4c + (gq >> 1))): o[2c][0, 2] for q = 0, 1 and o[2c + 1][0, 2] for
+        // q = 2, 3 (head h0; columns 1, 3 for h1).  The lane with the other parity
+        // (lane ^ 4) holds the rest; after one exchange the even lane writes b .. b + 3 and
+        // the odd lane b + 4 .. b + 7.
+        const int par = gq & 1;
+        float4 out0[4], out1[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float *lo = o[2 * c], *hi = o[2 * c + 1];
+            const float s0 = par ? lo[0] : hi[0], s1 = par ? lo[2] : hi[2];
+            const float s2 = par ? lo[1] : hi[1], s3 = par ? lo[3] : hi[3];
+            const float r0 = __shfl_xor_sync(0xffffffffu, s0, 4);
+            const float r1 = __shfl_xor_sync(0xffffffffu, s1, 4);
+            const float r2 = __shfl_xor_sync(0xffffffffu, s2, 4);
+            const float r3 = __shfl_xor_sync(0xffffffffu, s3, 4);
+            out0[c] = par ? make_float4(r0, hi[0], r1, hi[2]) : make_float4(lo[0], r0, lo[2], r1);
+            out1[c] = par ? make_float4(r2, hi[1], r3, hi[3]) : make_float4(lo[1], r2, lo[3], r3);
+        }
+        auto sh_off = [&](int c) { return 8 * gchunk(4 * c + (gq >> 1)) + 4 * par; };
+        if (h0 < G) {
+            if (gq == 0 && part == 0) {
+                ws_ml[2 * rec0] = m_run0;
+                ws_ml[2 * rec0 + 1] = l_run0;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<float4 *>(ws_o + rec0 * d + sh_off(c)) = out0[c];
+        }
+        if (h1 < G) {
+            if (gq == 0 && part == 0) {
+                ws_ml[2 * rec1] = m_run1;
+                ws_ml[2 * rec1 + 1] = l_run1;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<float4 *>(ws_o + rec1 * d + sh_off(c)) = out1[c];
+        }
+        return;
+    }
     if (h0 < G) {
         if (gq == 0 && part == 0) {
             ws_ml[2 * rec0] = m_run0;
@@ -463,8 +531,12 @@ cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int
     if (!attr_done) {
         for (const void *f : {reinterpret_cast<const void *>(decode_partial_kernel<1, false>),
                               reinterpret_cast<const void *>(decode_partial_kernel<2, false>),
-                              reinterpret_cast<const void *>(decode_partial_kernel<4, false>),
-                              reinterpret_cast<const void *>(decode_partial_kernel<1, true>),
+                              reinterpret_cast<const void *>(decode_partial_kernel<4, false>)}) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+            if (e != cudaSuccess) return e;
+        }
+        for (const void *f : {reinterpret_cast<const void *>(decode_partial_kernel<1, true>),
                               reinterpret_cast<const void *>(decode_partial_kernel<2, true>),
                               reinterpret_cast<const void *>(decode_partial_kernel<4, true>)}) {
             const cudaError_t e = cudaFuncSetAttribute(
