@@ -185,6 +185,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const int qpos = sv.R - 1;
     const int gq = lane >> 2, tq = lane & 3;
     const float2 *table = reinterpret_cast<const float2 *>(desc.rope);
+    // p-RoPE (§6.4), d = 512: a part whose 64 pairs never rotate -- table rows 0 and 1
+    // both exactly (1, 0), as gqa_rope_table_build writes for omega = 0 at amplitude 1 --
+    // neither copies table rows nor rotates its keys (the rotation would multiply them by
+    // 1 and add 0: the same keys).  With 64 of 256 pairs rotating this drops 3/4 of the
+    // table traffic, which at 2 KB per position otherwise overflows L2.  Warp-uniform.
+    // Not at d = 256, where the branches cost the register-bound kernel 5% on fully
+    // rotating rings.  (Rows read here, voted on after the query is loaded so the loads
+    // overlap.)
+    bool rot = true;
+    float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f), r1 = r0;
+    if constexpr (PARTS == 4) {
+        if (sv.R > 1) {
+            r0 = __ldg(reinterpret_cast<const float4 *>(table + 64 * part) + lane);
+            r1 = __ldg(reinterpret_cast<const float4 *>(table + d / 2 + 64 * part) + lane);
+        }
+    }
 
     // Q' as the B operand of S^T = K' Q'^T: thread (gq, tq) holds head gq, head-dim
     // elements 32c + 8tq + e (c = 0..3, e = 0..7); k-chunk kc = 2c + (e >> 2).
@@ -213,6 +229,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         }
     }
 
+    if constexpr (PARTS == 4) {
+        const bool id = r0.x == 1.f && r0.y == 0.f && r0.z == 1.f && r0.w == 0.f &&
+                        r1.x == 1.f && r1.y == 0.f && r1.z == 1.f && r1.w == 0.f;
+        rot = !__all_sync(0xffffffffu, id);
+    }
+
     float o[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -225,6 +247,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     float4 *stage_base = dsmem + (size_t)warp * 2 * 512;
     float *xchg = reinterpret_cast<float *>(dsmem + (size_t)kWarps * 2 * 512) +
                   (size_t)hg * (2 * parts * 32 * 4);
+
 
     const __nv_bfloat16 *kbase = static_cast<const __nv_bfloat16 *>(desc.k) + (size_t)g * sv.cap * d;
     const __nv_bfloat16 *vbase =
@@ -270,14 +293,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         float4 *stg = stage_base + (((kb - k_start) >> 4) & 1) * 512;
         const int kq = ((lane >> 4) << 2) | (lane & 3);   // 4c + qq
         const int lp_lo = (lane >> 2) & 3;                  // tq
+        if (rot) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int row = min(kb + i, k_end - 1);
-            const int k = ((i >> 3) << 3) | kq;
-            const int lp = ((i & 7) << 2) | lp_lo;
-            cp_async16(stg + k * 32 + (lp ^ ((k & 3) << 1)),
-                       reinterpret_cast<const float4 *>(table + (size_t)row * (d / 2) +
-                                                        64 * part) + lane);
+            for (int i = 0; i < 16; ++i) {
+                const int row = min(kb + i, k_end - 1);
+                const int k = ((i >> 3) << 3) | kq;
+                const int lp = ((i & 7) << 2) | lp_lo;
+                cp_async16(stg + k * 32 + (lp ^ ((k & 3) << 1)),
+                           reinterpret_cast<const float4 *>(table + (size_t)row * (d / 2) +
+                                                            64 * part) + lane);
+            }
         }
         cp_async_commit();
     };
@@ -314,13 +339,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             }
         }
         // rotate K at logical positions kb + gq, kb + gq + 8 (clamped rows: k_end - 1)
+        if (rot) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 2; ++c) {
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                const int sw = lane ^ (qq << 1);
-                rotate_word(bl.k0[c], bl.k0[c + 2], qq, stg[(4 * c + qq) * 32 + sw]);
-                rotate_word(bl.k1[c], bl.k1[c + 2], qq, stg[(8 + 4 * c + qq) * 32 + sw]);
+                for (int qq = 0; qq < 4; ++qq) {
+                    const int sw = lane ^ (qq << 1);
+                    rotate_word(bl.k0[c], bl.k0[c + 2], qq, stg[(4 * c + qq) * 32 + sw]);
+                    rotate_word(bl.k1[c], bl.k1[c + 2], qq, stg[(8 + 4 * c + qq) * 32 + sw]);
+                }
             }
         }
         // S^T (16 keys x 8 heads) in two independent accumulation chains

@@ -192,6 +192,35 @@ def test_wide_head_decode(Hq, Hkv, d):
     gu.compare(lse, rl, what="decode lse")
 
 
+def test_prope_unrotated_parts_match_rotation():
+    """d = 512 with p-RoPE: a part whose 64 pairs never rotate (table rows 0 and 1 both
+    (1, 0)) skips the table rows and the rotation.  Forcing the rotation on those parts --
+    row 1 of pairs 64..255 given sin = 1e-30, which leaves every bf16 key of a normal
+    sample as it is -- gives the same output and lse bit for bit."""
+    gu.require_gpu()
+    Hq, Hkv, d = 16, 2, 512
+    x = _random_batch([5, 700, 2100], [], Hq, Hkv, d, seed=4242)
+    x = replace(x, rope=[PROPE] * 3)
+    st = DecodeSetup(x, d)
+    scale = 1 / math.sqrt(d)
+    o1, lse1, _ = run_step(st, Hq, Hkv, scale, max_len=4096)
+    tab, n = st.tables[PROPE]
+    t2 = tab.clone().view(n, d // 2, 2)
+    t2[1, 64:, 1] = 1e-30
+    t2 = t2.view(-1)
+    a = gqa.make_kv_descs(st.kc, st.vc, [t2] * 3, x.cap, st.counts().tolist(), x.is_ring,
+                          [n] * 3)
+    descs2 = torch.from_numpy(a.view(np.uint8).copy()).cuda()
+    o2 = torch.empty_like(st.q)
+    lse2 = torch.empty_like(lse1)
+    wsb = gqa.gqa_decode_workspace_bytes(3, Hq, d, 4096)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    gqa.gqa_attn_decode(st.q, descs2, 3, Hq, Hkv, d, scale, 4096, o2, lse2, ws, wsb)
+    assert gqa.gqa_get_device_status() == 0
+    assert torch.equal(o1, o2)
+    assert torch.equal(lse1, lse2)
+
+
 def test_long_split_boundaries():
     """max_len > 4096 (2048-key splits): caches ending just before, at and after split
     boundaries, a split that holds a single key, and rings that wrap."""
