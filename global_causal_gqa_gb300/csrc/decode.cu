@@ -6,9 +6,10 @@
 // 4 Hkv d bytes per token and layer -- the bound this kernel is written against).
 //
 // Work split: one CTA per (split of decode_chunk(max_len) keys, sequence, block of KV
-// heads); each
-// KV head is streamed by d/128 warps (d = 128, 256, 512), each of which owns the pairs
-// [64 p, 64 p + 64) of the split-half RoPE -- head-dim elements 64p.. and d/2 + 64p.. -- so
+// heads); each KV head is streamed by d/128 warps (d = 128, 256, 512), each of which owns
+// 64 pairs of the split-half RoPE in two groups of 32 -- [64 p, 64 p + 64) at d <= 256;
+// [32 p, +32) and [d/4 + 32 p, +32) at d = 512, so that the pairs p-RoPE rotates are
+// spread over two warps -- with the head-dim elements j and d/2 + j of each pair j, so
 // every warp sees a 128-element vector whose RoPE pairs are (l, l + 64), the d = 128
 // layout.  Keys go in blocks of 16 with 16-byte read-only loads, double-buffered in
 // registers so the next block's loads are in flight during the math; the warps of a
@@ -166,8 +167,24 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const int hg = warp / parts;                 // head group within the CTA
     const int g = blockIdx.z * (kWarps / parts) + hg;
     // global 16-byte chunk of the row for local chunk lc (8 elements) of this warp
-    auto gchunk = [&](int lc) {
+    // This warp's RoPE pairs for the K/Q layout's chunk group c (c = 0, 1): 32 pairs from
+    // pb(c).  d = 512 spreads them, [32 part, +32) and [d/4 + 32 part, +32), so that the 64
+    // pairs p-RoPE rotates fall to two warps, half each; otherwise [64 part + 32 c, +32).
+    constexpr bool kSpread = PARTS == 4;
+    auto pb = [&](int c) { return kSpread ? 32 * part + c * (d / 4) : 64 * part + 32 * c; };
+    // global 16-byte chunk of the row for local chunk lc (8 elements) of this warp: K and Q
+    // (gchunk), and V of separate caches (vchunk, whose 8 first-half chunks are one
+    // 128-byte line)
+    auto vchunk = [&](int lc) {
         return lc < 8 ? 8 * part + lc : d / 16 + 8 * part + (lc - 8);
+    };
+    auto gchunk = [&](int lc) {
+        if constexpr (kSpread) {
+            const int l = lc & 7;
+            return (lc >> 3) * (d / 16) + pb(l >> 2) / 8 + (l & 3);
+        } else {
+            return vchunk(lc);
+        }
     };
     const gqa_kv_desc desc = descs[seq];
     const SeqView sv = seq_view(desc, max_len);
@@ -185,20 +202,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const int qpos = sv.R - 1;
     const int gq = lane >> 2, tq = lane & 3;
     const float2 *table = reinterpret_cast<const float2 *>(desc.rope);
-    // p-RoPE (§6.4), d = 512: a part whose 64 pairs never rotate -- table rows 0 and 1
+    // p-RoPE (§6.4), d = 512: a group of 32 pairs that never rotate -- table rows 0 and 1
     // both exactly (1, 0), as gqa_rope_table_build writes for omega = 0 at amplitude 1 --
     // neither copies table rows nor rotates its keys (the rotation would multiply them by
     // 1 and add 0: the same keys).  With 64 of 256 pairs rotating this drops 3/4 of the
-    // table traffic, which at 2 KB per position otherwise overflows L2.  Warp-uniform.
-    // Not at d = 256, where the branches cost the register-bound kernel 5% on fully
-    // rotating rings.  (Rows read here, voted on after the query is loaded so the loads
-    // overlap.)
-    bool rot = true;
+    // table traffic, which at 2 KB per position otherwise overflows L2, and the rotation
+    // left falls to two warps.  rot_c: group c rotates (warp-uniform); lanes 16c .. 16c + 15
+    // read its rows 0 and 1 here, and the vote follows the query load so the loads
+    // overlap.  Not at d = 256, where the branches cost the register-bound kernel 5% on
+    // fully rotating rings.
+    bool rot0 = true, rot1 = true;
     float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f), r1 = r0;
     if constexpr (PARTS == 4) {
         if (sv.R > 1) {
-            r0 = __ldg(reinterpret_cast<const float4 *>(table + 64 * part) + lane);
-            r1 = __ldg(reinterpret_cast<const float4 *>(table + d / 2 + 64 * part) + lane);
+            const float2 *t0 = table + pb(lane >> 4) + 2 * (lane & 15);
+            r0 = __ldg(reinterpret_cast<const float4 *>(t0));
+            r1 = __ldg(reinterpret_cast<const float4 *>(t0 + d / 2));
         }
     }
 
@@ -215,7 +234,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
             for (int c = 0; c < 2; ++c)
                 rotate8(qc[c], qc[c + 2],
-                        table + (size_t)qpos * (d / 2) + 64 * part + 32 * c + 8 * tq);
+                        table + (size_t)qpos * (d / 2) +
+                            (kSpread ? pb(c) : 64 * part + 32 * c) + 8 * tq);
         } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c) qc[c] = make_uint4(0, 0, 0, 0);
@@ -232,7 +252,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     if constexpr (PARTS == 4) {
         const bool id = r0.x == 1.f && r0.y == 0.f && r0.z == 1.f && r0.w == 0.f &&
                         r1.x == 1.f && r1.y == 0.f && r1.z == 1.f && r1.w == 0.f;
-        rot = !__all_sync(0xffffffffu, id);
+        const unsigned b = __ballot_sync(0xffffffffu, id);
+        rot0 = (b & 0xFFFFu) != 0xFFFFu;
+        rot1 = (b >> 16) != 0xFFFFu;
     }
 
     float o[8][4];
@@ -283,8 +305,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                 const int key = min(kb + 2 * tq + (i & 1) + ((i >> 1) << 3), k_end - 1);
                 const uint4 *vr =
                     reinterpret_cast<const uint4 *>(vbase + (size_t)slot_of(key) * d);
-                bl.vv[i][0] = ld_stream(vr + gchunk(gq));
-                bl.vv[i][1] = ld_stream(vr + gchunk(8 + gq));
+                bl.vv[i][0] = ld_stream(vr + vchunk(gq));
+                bl.vv[i][1] = ld_stream(vr + vchunk(8 + gq));
             }
         }
         // table rows kb .. kb + 15: instruction i copies row i (clamped), lane = 16-byte
@@ -293,7 +315,20 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         float4 *stg = stage_base + (((kb - k_start) >> 4) & 1) * 512;
         const int kq = ((lane >> 4) << 2) | (lane & 3);   // 4c + qq
         const int lp_lo = (lane >> 2) & 3;                  // tq
-        if (rot) {
+        // lane = 16-byte piece l & 15 of chunk group l >> 4
+        if constexpr (kSpread) {
+            if (lane < 16 ? rot0 : rot1) {
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(table + pb(lane >> 4)) + (lane & 15);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int row = min(kb + i, k_end - 1);
+                    const int k = ((i >> 3) << 3) | kq;
+                    const int lp = ((i & 7) << 2) | lp_lo;
+                    cp_async16(stg + k * 32 + (lp ^ ((k & 3) << 1)), src + (size_t)row * (d / 4));
+                }
+            }
+        } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int row = min(kb + i, k_end - 1);
@@ -339,9 +374,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             }
         }
         // rotate K at logical positions kb + gq, kb + gq + 8 (clamped rows: k_end - 1)
-        if (rot) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 2; ++c) {
+            if (c == 0 ? rot0 : rot1) {
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
                     const int sw = lane ^ (qq << 1);

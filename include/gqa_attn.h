@@ -119,7 +119,7 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
  * One descriptor per sequence, in device memory, owned by the caller.
  *   k, v   : device [Hkv, cap, d] bf16, K stored before RoPE.
  *   rope   : device RoPE table for this sequence's layer type; rope_len positions.
- *            Decode at d = 512 treats a 64-pair slice whose rows 0 and 1 are both
+ *            Decode at d = 512 treats a group of 32 pairs whose rows 0 and 1 are all
  *            exactly (1, 0) as never rotating (omega = 0 at amplitude 1, as
  *            gqa_rope_table_build writes p-RoPE's unrotated pairs) and reads no further
  *            rows of it.
