@@ -501,8 +501,9 @@ def e2e_decode(w, st, steps, warmup, stream, kv_bytes):
 def bench_decode_model(w, steps, warmup, stream, peaks, peak_src):
     """One step = kv_append + decode for every layer (7 local ring layers then 1 global
     linear layer per period), captured once in a CUDA graph and replayed.  Caches and
-    inputs are drawn on the device (synthetic N(0,1), seeded); the descriptor counts are
-    restored at the start of every replay so each step appends into the same slots.
+    inputs are drawn on the device (synthetic N(0,1), seeded); every layer's descriptors
+    live in one buffer whose counts are restored by a single copy at the start of each
+    replay, so each step appends into the same slots.
     Reported against the pages' byte model: K and V read once per (sequence, KV head),
     4 Hkv d [n_global N + n_local min(N, W)] bytes per sequence."""
     import numpy as np
@@ -519,6 +520,7 @@ def bench_decode_model(w, steps, warmup, stream, peaks, peak_src):
         gqa.gqa_rope_table_build(t, f, w.d, rope.amp, n)
         tables[is_g] = (t, n)
     layers = []
+    desc_rows = []
     for l in range(w.layers):
         is_g = (l % w.period) == w.period - 1
         cap = w.N if is_g else w.W
@@ -528,12 +530,16 @@ def bench_decode_model(w, steps, warmup, stream, peaks, peak_src):
         a = gqa.make_kv_descs([kc[i] for i in range(w.nseq)], [vc[i] for i in range(w.nseq)],
                               [tab] * w.nseq, [cap] * w.nseq, [w.N - 1] * w.nseq,
                               [0 if is_g else 1] * w.nseq, [tlen] * w.nseq)
-        d0 = torch.from_numpy(a.view(np.uint8).copy()).cuda()
-        layers.append({"kc": kc, "vc": vc, "descs0": d0, "descs": d0.clone(),
+        desc_rows.append(torch.from_numpy(a.view(np.uint8).copy()))
+        layers.append({"kc": kc, "vc": vc,
                        "q": rnd(w.nseq, w.Hq, w.d), "k_new": rnd(w.nseq, w.Hkv, w.d),
                        "v_new": rnd(w.nseq, w.Hkv, w.d), "o": torch.empty(w.nseq, w.Hq, w.d,
                                                                           dtype=torch.bfloat16,
                                                                           device="cuda")})
+    descs0 = torch.stack(desc_rows).cuda()     # [layers, nseq * sizeof(gqa_kv_desc)]
+    descs = descs0.clone()
+    for l, L in enumerate(layers):
+        L["descs"] = descs[l]                   # contiguous row: this layer's array
     max_len = w.N
     wsb = gqa.gqa_decode_workspace_bytes(w.nseq, w.Hq, w.d, max_len)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
@@ -543,8 +549,8 @@ def bench_decode_model(w, steps, warmup, stream, peaks, peak_src):
     assert bytes_step == w.nseq * acc.kv_bytes_per_token(w.layers, w.Hkv, w.d, w.N, w.W)
 
     def body():
+        descs.copy_(descs0, non_blocking=True)
         for L in layers:
-            L["descs"].copy_(L["descs0"], non_blocking=True)
             gqa.gqa_kv_append(L["descs"], w.nseq, L["k_new"], L["v_new"], w.Hkv, w.d, None)
             gqa.gqa_attn_decode(L["q"], L["descs"], w.nseq, w.Hq, w.Hkv, w.d, w.scale, max_len,
                                 L["o"], None, ws, wsb)

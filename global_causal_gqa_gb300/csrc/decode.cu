@@ -153,6 +153,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                           float *__restrict__ ws_o, int *status,
                           const float *__restrict__ k_gamma) {
     constexpr int d = kD * PARTS, parts = PARTS;
+    griddep_wait();               // the appended token, counts and partials of earlier kernels
+    griddep_launch_dependents();  // the combine kernel may start launching
     extern __shared__ float4 dsmem[];
     uint4 *sgain = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(dsmem) + kDecodeSmem);
     if constexpr (SHARED) {
@@ -555,6 +557,8 @@ __global__ void __launch_bounds__(kMaxHeadDim)
                           const float *__restrict__ ws_o, __nv_bfloat16 *__restrict__ out,
                           float *__restrict__ lse) {
     const int h = blockIdx.x, seq = blockIdx.y, dd = threadIdx.x;
+    griddep_wait();               // this step's partials
+    griddep_launch_dependents();
     const SeqView sv = seq_view(descs[seq], max_len);
     if (!sv.ok) return;
     const int chunk = decode_chunk(max_len);
@@ -614,15 +618,14 @@ cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int
                        : (parts == 1   ? decode_partial_kernel<1, false>
                           : parts == 2 ? decode_partial_kernel<2, false>
                                        : decode_partial_kernel<4, false>);
-    kern<<<grid, heads * parts * 32, shared ? kDecodeSmemShared : kDecodeSmem, s>>>(
-        static_cast<const __nv_bfloat16 *>(q), descs, Hq, Hkv, scale_log2, max_len, nsplit,
-        ws_ml, ws_o, status, k_gamma);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(kern, grid, dim3(heads * parts * 32),
+                               shared ? kDecodeSmemShared : kDecodeSmem, s,
+                               static_cast<const __nv_bfloat16 *>(q), descs, Hq, Hkv,
+                               scale_log2, max_len, nsplit, ws_ml, ws_o, status, k_gamma);
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<<<dim3(Hq, nseq), d, 0, s>>>(descs, Hq, d, max_len, nsplit, ws_ml,
-                                                        ws_o, static_cast<__nv_bfloat16 *>(o),
-                                                        lse);
-    return cudaGetLastError();
+    return launch_pdl(decode_combine_kernel, dim3(Hq, nseq), dim3(d), 0, s, descs, Hq, d,
+                      max_len, nsplit, static_cast<const float *>(ws_ml),
+                      static_cast<const float *>(ws_o), static_cast<__nv_bfloat16 *>(o), lse);
 }
 
 }  // namespace gqa

@@ -13,6 +13,34 @@ struct InvFreq {
     double w[kMaxHeadDim / 2];
 };
 
+// Launches `kern` with programmatic stream serialization: its blocks may be scheduled
+// while the previous kernel on the stream drains, so the launch latency overlaps that
+// kernel's tail.  The kernel must call griddep_wait() before it reads anything an earlier
+// kernel on the stream wrote (the decode step's append -> partial -> combine chain).
+// Not while the stream is being captured into a CUDA graph: a graph already launches
+// back to back, and with programmatic edges the 64-layer decode step ran 1% slower
+// (eagerly it runs 7% faster with them).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+        (void)cudaGetLastError();   // treat as capturing: plain stream order
+        cap = cudaStreamCaptureStatusActive;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cap == cudaStreamCaptureStatusNone ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // RoPE table and application (rope.cu)
 cudaError_t launch_rope_table(float *table, const InvFreq &w, int d, double amp, int max_pos,
                               cudaStream_t s);

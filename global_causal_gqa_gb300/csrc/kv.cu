@@ -17,6 +17,8 @@ __global__ void kv_append_kernel(gqa_kv_desc *descs, const uint4 *__restrict__ k
                                  const uint4 *__restrict__ v_new, int Hkv, int d,
                                  int32_t *slots, int *status) {
     __shared__ int s_slot;
+    griddep_wait();               // the descriptors and caches of earlier kernels
+    griddep_launch_dependents();  // the decode kernels may start launching
     const int seq = blockIdx.x;
     gqa_kv_desc *desc = descs + seq;
     if (threadIdx.x == 0) {
@@ -55,10 +57,9 @@ __global__ void kv_append_kernel(gqa_kv_desc *descs, const uint4 *__restrict__ k
 cudaError_t launch_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new,
                              const void *v_new, int Hkv, int d, int32_t *slots, int *status,
                              cudaStream_t s) {
-    kv_append_kernel<<<nseq, 128, 0, s>>>(descs, static_cast<const uint4 *>(k_new),
-                                          static_cast<const uint4 *>(v_new), Hkv, d, slots,
-                                          status);
-    return cudaGetLastError();
+    return launch_pdl(kv_append_kernel, dim3(nseq), dim3(128), 0, s, descs,
+                      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), Hkv,
+                      d, slots, status);
 }
 
 }  // namespace gqa

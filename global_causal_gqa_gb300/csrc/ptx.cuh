@@ -311,6 +311,18 @@ __device__ __forceinline__ void reg_dealloc() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// ---- programmatic dependent launch ----------------------------------------------------------
+// A kernel launched with programmatic stream serialization may start before the previous
+// kernel on its stream has finished: griddep_wait() returns once that kernel has completed
+// and its writes are visible (at once when there is no such dependency), and
+// griddep_launch_dependents() lets the next kernel start launching.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- misc ----------------------------------------------------------------------------------
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
