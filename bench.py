@@ -59,10 +59,22 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_sha256(path: str) -> str:
+    """SHA-256 of a C/CUDA source's code: comments, trailing blanks and empty lines
+    removed, so that editing a comment keeps a measurement of the code valid."""
+    import re
+    with open(path) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    lines = [ln.rstrip() for ln in src.splitlines()]
+    return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
+
+
 def traffic_record(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` on `workload` from a committed ncu capture
-    (profiles/traffic.json), valid only while the kernel source is byte-identical to the
-    one profiled; None otherwise."""
+    (profiles/traffic.json), valid only while the kernel source's code is identical to
+    the one profiled (code_sha256); None otherwise."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -70,9 +82,8 @@ def traffic_record(kernel: str, workload: str):
         rec = json.load(f).get(kernel, {}).get(workload)
     if not rec:
         return None
-    with open(os.path.join(ROOT, "global_causal_gqa_gb300", "csrc", rec["source"]), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
-    return rec["bytes_per_launch"] if rec.get("source_sha256") == sha else None
+    sha = code_sha256(os.path.join(ROOT, "global_causal_gqa_gb300", "csrc", rec["source"]))
+    return rec["bytes_per_launch"] if rec.get("code_sha256") == sha else None
 
 
 def kernel_name(L) -> str:

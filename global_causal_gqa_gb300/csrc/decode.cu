@@ -165,10 +165,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     const int split = blockIdx.x, seq = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int part = warp % parts;               // this warp's RoPE pairs: [64 part, +64)
+    const int part = warp % parts;               // this warp's 64 RoPE pairs (pb below)
     const int hg = warp / parts;                 // head group within the CTA
     const int g = blockIdx.z * (kWarps / parts) + hg;
-    // global 16-byte chunk of the row for local chunk lc (8 elements) of this warp
     // This warp's RoPE pairs for the K/Q layout's chunk group c (c = 0, 1): 32 pairs from
     // pb(c).  d = 512 spreads them, [32 part, +32) and [d/4 + 32 part, +32), so that the 64
     // pairs p-RoPE rotates fall to two warps, half each; otherwise [64 part + 32 c, +32).
@@ -223,8 +222,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         }
     }
 
-    // Q' as the B operand of S^T = K' Q'^T: thread (gq, tq) holds head gq, head-dim
-    // elements 32c + 8tq + e (c = 0..3, e = 0..7); k-chunk kc = 2c + (e >> 2).
+    // Q' as the B operand of S^T = K' Q'^T: thread (gq, tq) holds head gq, elements
+    // 32c + 8tq + e (c = 0..3, e = 0..7) of this warp's 128 (global chunk gchunk(4c + tq));
+    // k-chunk kc = 2c + (e >> 2).
     uint32_t qb[8][2];
     {
         uint4 qc[4];
@@ -266,12 +266,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
     // This warp's two table stages: the 16 table rows of a key block, 16-byte entry
     // (k, lane) at k * 32 + (lane ^ 2 (k & 3)) holding what lane (gq, tq) needs for
-    // k = 8 rs + 4 c + qq: pairs 32c + 8tq + 2qq and the next one at position kb + gq + 8 rs.
+    // k = 8 rs + 4 c + qq: pairs pb(c) + 8tq + 2qq and the next one at position
+    // kb + gq + 8 rs.
     // The XOR keeps both the copies in and the reads out free of bank conflicts.
     float4 *stage_base = dsmem + (size_t)warp * 2 * 512;
     float *xchg = reinterpret_cast<float *>(dsmem + (size_t)kWarps * 2 * 512) +
                   (size_t)hg * (2 * parts * 32 * 4);
-
 
     const __nv_bfloat16 *kbase = static_cast<const __nv_bfloat16 *>(desc.k) + (size_t)g * sv.cap * d;
     const __nv_bfloat16 *vbase =
@@ -282,11 +282,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     };
 
     // One block = 16 keys: K rows kb + gq and kb + gq + 8, V rows kb + 2tq + {0, 1, 8, 9}
-    // (16-byte chunks gq and 8 + gq of each, so every load instruction reads whole
-    // 128-byte lines), and the block's table rows copied to shared memory; rows at or
-    // past k_end are clamped in range and get weight 0.  Two register buffers and two
-    // table stages: the next block's loads are in flight while the current block is
-    // computed.
+    // (16-byte chunks vchunk(gq) and vchunk(8 + gq) of each, so every load instruction
+    // reads whole 128-byte lines), and the block's table rows copied to shared memory;
+    // rows at or past k_end are clamped in range and get weight 0.  Two register buffers
+    // and two table stages: the next block's loads are in flight while the current block
+    // is computed.
     struct Block {
         uint4 k0[4], k1[4], vv[4][2];
         int kb;
@@ -311,13 +311,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                 bl.vv[i][1] = ld_stream(vr + vchunk(8 + gq));
             }
         }
-        // table rows kb .. kb + 15: instruction i copies row i (clamped), lane = 16-byte
-        // piece of the row, i.e. pairs 2 lane, 2 lane + 1 = 32c + 8tq + 2qq
+        // table rows kb .. kb + 15: instruction i copies row i (clamped); lane l copies the
+        // 16-byte piece l & 15 of chunk group c = l >> 4 -- pairs pb(c) + 2 (l & 15) and the
+        // next one, i.e. pb(c) + 8tq + 2qq -- skipped for a group that never rotates
         __syncwarp();   // every lane is done reading this stage's previous block
         float4 *stg = stage_base + (((kb - k_start) >> 4) & 1) * 512;
         const int kq = ((lane >> 4) << 2) | (lane & 3);   // 4c + qq
         const int lp_lo = (lane >> 2) & 3;                  // tq
-        // lane = 16-byte piece l & 15 of chunk group l >> 4
         if constexpr (kSpread) {
             if (lane < 16 ? rot0 : rot1) {
                 const float4 *src =

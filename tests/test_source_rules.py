@@ -2,9 +2,10 @@
 
 A kernel launched with programmatic stream serialization (`launch_pdl`) may start while
 the previous kernel on the stream is still writing its inputs; it must execute
-`griddep_wait()` before it reads any memory.  This test finds every kernel that
+`griddep_wait()` before it reads any memory.  One test finds every kernel that
 `launch_pdl` can launch and checks that `griddep_wait();` comes first in its body, with
-nothing before it that indexes or dereferences memory."""
+nothing before it that indexes or dereferences memory.  Another checks the code hash that
+keys the committed DRAM-traffic measurements."""
 import os
 import re
 
@@ -79,3 +80,18 @@ def test_pdl_kernel_waits_before_reading(name):
     before = body[:k]
     assert "[" not in before and "->" not in before, \
         f"{name} touches memory before griddep_wait(): {before.strip()!r}"
+
+
+def test_code_hash_ignores_comments_only(tmp_path):
+    """The DRAM-traffic records are keyed on the hash of a source's code: a comment or
+    blank-line edit keeps it, any code edit changes it."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    a = tmp_path / "a.cu"
+    a.write_text("// head\n__global__ void k(int *p) {\n    p[0] = 1;  // store\n}\n")
+    h = bench.code_sha256(str(a))
+    a.write_text("/* other\n   words */\n__global__ void k(int *p) {\n\n    p[0] = 1;\n}\n")
+    assert bench.code_sha256(str(a)) == h
+    a.write_text("__global__ void k(int *p) {\n    p[0] = 2;\n}\n")
+    assert bench.code_sha256(str(a)) != h
