@@ -27,6 +27,12 @@
  *   - Errors found on the device (a bounded wait that expired, a full cache, an index
  *     out of range) are recorded in the device status word and returned by the next
  *     gqa_get_device_status().  Device code never traps.
+ *   - Stream order holds as for any kernel.  On a stream that is not being captured,
+ *     gqa_kv_append and the decode calls launch with programmatic stream serialization
+ *     and let the next kernel begin launching early.  Each of their kernels waits for its
+ *     predecessor before reading.  A caller's own kernel launched after them with that
+ *     attribute must likewise execute griddepcontrol.wait (cudaGridDependencySynchronize)
+ *     before it reads their outputs.
  *   - Head dims: prefill and decode d in {128, 256, 512}; kv_append, rope_apply and the
  *     Q/K normalisation d in {64, 128, 256, 512}.  Query group G = Hq/Hkv must be an
  *     integer; decode needs G <= 8.  Other values return GQA_ERR_UNSUPPORTED.
