@@ -13,7 +13,9 @@
 // projection output Z gives K = RoPE(N_{gamma_k}(Z)) and V = N_1(Z).  The cache stores
 // only Zn = bf16(N_1(Z)); since N_gamma(Z) = gamma * N_1(Z), the keys are recomputed from
 // it as RoPE(bf16(bf16(gamma_k) * Zn)) -- the gain applied in bf16 to the stored row,
-// exactly as the decode kernel applies it -- so prefill and decode see the same keys.
+// exactly as the decode kernel applies it -- so prefill and decode rotate the same bf16
+// keys (the rotation's two products may round in a different order: at most one bf16
+// step apart).
 //
 // One warp per row.  Lane l holds the 32-bit words (bf16 pairs) l, l + 32, ... of the
 // row's first half and the words d/4 later of the second half, so each RoPE pair
