@@ -8,6 +8,8 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "gqa_attn.h"
 #include "internal.h"
@@ -50,6 +52,23 @@ gqa_status from_cuda(cudaError_t e) {
 }
 
 }  // namespace
+
+namespace gqa {
+
+cudaError_t ensure_smem_attr(const void *func, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;   // (kernel, device)
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({func, dev})) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert({func, dev});
+    return e;
+}
+
+}  // namespace gqa
 
 extern "C" {
 
@@ -127,7 +146,7 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
                             float scale, const float *table, int table_len, int k_is_rotated,
                             void *workspace, size_t workspace_bytes, gqa_stream_t stream) {
     if (!q || !k || !v || !o || !table || B <= 0 || T <= 0 || S <= 0 || T > S || Hq <= 0 ||
-        Hkv <= 0 || (Hq % Hkv) != 0 || !std::isfinite(scale))
+        Hkv <= 0 || (Hq % Hkv) != 0 || !(scale > 0.f) || !std::isfinite(scale))
         return GQA_ERR_INVALID_ARG;
     if (d != 128 && d != 256 && d != 512) return GQA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(table) ||
@@ -285,15 +304,16 @@ gqa_status gqa_kv_shared_append(gqa_kv_desc *descs, int nseq, const void *q, con
 
 size_t gqa_decode_workspace_bytes(int nseq, int Hq, int d, int max_len) {
     if (nseq <= 0 || Hq <= 0 || d <= 0 || max_len <= 0) return 0;
-    const size_t ns = static_cast<size_t>(gqa::decode_num_splits(max_len));
-    return static_cast<size_t>(nseq) * Hq * ns * (d + 2) * sizeof(float);
+    const int ns = gqa::decode_num_splits(max_len);
+    return (gqa::decode_ml_floats(nseq, Hq, ns) + static_cast<size_t>(nseq) * Hq * ns * d) *
+           sizeof(float);
 }
 
 gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
                            int d, float scale, int max_len, void *o, float *lse,
                            void *workspace, size_t workspace_bytes, gqa_stream_t stream) {
     if (!q || !descs || !o || nseq <= 0 || Hq <= 0 || Hkv <= 0 || (Hq % Hkv) != 0 ||
-        max_len <= 0 || !std::isfinite(scale))
+        max_len <= 0 || !(scale > 0.f) || !std::isfinite(scale))
         return GQA_ERR_INVALID_ARG;
     if ((d != 128 && d != 256 && d != 512) || Hq / Hkv > 8) return GQA_ERR_UNSUPPORTED;
     if (nseq > 65535) return GQA_ERR_UNSUPPORTED;
@@ -315,7 +335,7 @@ gqa_status gqa_attn_decode_kv_shared(const void *q, const gqa_kv_desc *descs, in
                                      int max_len, void *o, float *lse, void *workspace,
                                      size_t workspace_bytes, gqa_stream_t stream) {
     if (!q || !descs || !o || !k_gamma || nseq <= 0 || Hq <= 0 || Hkv <= 0 ||
-        (Hq % Hkv) != 0 || max_len <= 0 || !std::isfinite(scale))
+        (Hq % Hkv) != 0 || max_len <= 0 || !(scale > 0.f) || !std::isfinite(scale))
         return GQA_ERR_INVALID_ARG;
     if ((d != 128 && d != 256 && d != 512) || Hq / Hkv > 8) return GQA_ERR_UNSUPPORTED;
     if (nseq > 65535) return GQA_ERR_UNSUPPORTED;
@@ -364,7 +384,7 @@ gqa_status gqa_attn_decode_static(const void *q, const gqa_kv_desc *descs, int n
                                   int Hkv, int d, float scale, int max_len, void *o,
                                   float *lse, gqa_stream_t stream) {
     if (!q || !descs || !o || nseq <= 0 || Hq <= 0 || Hkv <= 0 || (Hq % Hkv) != 0 ||
-        max_len <= 0 || !std::isfinite(scale))
+        max_len <= 0 || !(scale > 0.f) || !std::isfinite(scale))
         return GQA_ERR_INVALID_ARG;
     if ((d != 128 && d != 256 && d != 512) || Hq / Hkv > 8) return GQA_ERR_UNSUPPORTED;
     if (nseq > 65535) return GQA_ERR_UNSUPPORTED;

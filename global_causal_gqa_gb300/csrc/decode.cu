@@ -587,30 +587,12 @@ cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int
                           int *status, cudaStream_t s, const float *k_gamma) {
     const int nsplit = decode_num_splits(max_len);
     float *ws_ml = ws;
-    float *ws_o = ws + (size_t)2 * nseq * Hq * nsplit;
+    float *ws_o = ws + decode_ml_floats(nseq, Hq, nsplit);   // 16-byte aligned
     const int parts = d / kD;                       // warps per KV head
     const int heads_per_cta = kWarps / parts;
     const int heads = Hkv < heads_per_cta ? Hkv : heads_per_cta;
     dim3 grid(nsplit, nseq, (Hkv + heads_per_cta - 1) / heads_per_cta);
     const float scale_log2 = scale * 1.4426950408889634f;
-    static bool attr_done = false;
-    if (!attr_done) {
-        for (const void *f : {reinterpret_cast<const void *>(decode_partial_kernel<1, false>),
-                              reinterpret_cast<const void *>(decode_partial_kernel<2, false>),
-                              reinterpret_cast<const void *>(decode_partial_kernel<4, false>)}) {
-            const cudaError_t e =
-                cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
-            if (e != cudaSuccess) return e;
-        }
-        for (const void *f : {reinterpret_cast<const void *>(decode_partial_kernel<1, true>),
-                              reinterpret_cast<const void *>(decode_partial_kernel<2, true>),
-                              reinterpret_cast<const void *>(decode_partial_kernel<4, true>)}) {
-            const cudaError_t e = cudaFuncSetAttribute(
-                f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmemShared);
-            if (e != cudaSuccess) return e;
-        }
-        attr_done = true;
-    }
     const bool shared = k_gamma != nullptr;
     auto kern = shared ? (parts == 1   ? decode_partial_kernel<1, true>
                           : parts == 2 ? decode_partial_kernel<2, true>
@@ -618,8 +600,10 @@ cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int
                        : (parts == 1   ? decode_partial_kernel<1, false>
                           : parts == 2 ? decode_partial_kernel<2, false>
                                        : decode_partial_kernel<4, false>);
-    cudaError_t e = launch_pdl(kern, grid, dim3(heads * parts * 32),
-                               shared ? kDecodeSmemShared : kDecodeSmem, s,
+    const int smem = shared ? kDecodeSmemShared : kDecodeSmem;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(kern, grid, dim3(heads * parts * 32), smem, s,
                                static_cast<const __nv_bfloat16 *>(q), descs, Hq, Hkv,
                                scale_log2, max_len, nsplit, ws_ml, ws_o, status, k_gamma);
     if (e != cudaSuccess) return e;

@@ -65,6 +65,17 @@ __host__ __device__ inline int decode_chunk(int max_len) {
     return max_len > 4096 ? kDecodeChunkLong : kDecodeChunkShort;
 }
 int decode_num_splits(int max_len);
+// Decode workspace layout: nseq Hq nsplit (m, l) float pairs, padded to a multiple of 4
+// floats so that the O partials after them start on a 16-byte boundary (the partial
+// kernel writes them with 16-byte stores), then nseq Hq nsplit rows of d floats.
+__host__ __device__ inline size_t decode_ml_floats(int nseq, int Hq, int nsplit) {
+    const size_t n = (size_t)2 * nseq * Hq * nsplit;
+    return (n + 3) & ~(size_t)3;
+}
+// Raises `func`'s dynamic shared-memory limit to `bytes` on the current device, once per
+// (kernel, device): the attribute belongs to a device's context, so each GPU a process
+// drives needs its own call.  Thread-safe.
+cudaError_t ensure_smem_attr(const void *func, int bytes);
 // k_gamma == nullptr: separate K and V caches; otherwise each desc.k holds Zn of a shared
 // K/V projection (keys RoPE(bf16(gamma_k) * Zn), values Zn) and desc.v is not read
 cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,

@@ -499,13 +499,9 @@ int launch_prefill_stream(const void *q, const void *k_rot, const void *v, void 
     if (!make_map(&mq, q, d, T, B * Hq) || !make_map(&mk, k_rot, d, S, B * Hkv) ||
         !make_map(&mv, v, d, S, B * Hkv))
         return GQA_ERR_CUDA;
-    static bool attr_done = false;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess)
-            return GQA_ERR_CUDA;   // the error stays readable with cudaGetLastError
-        attr_done = true;
-    }
+    if (ensure_smem_attr(reinterpret_cast<const void *>(prefill_kernel), kSmemBytes) !=
+        cudaSuccess)
+        return GQA_ERR_CUDA;   // the error stays readable with cudaGetLastError
     Params p;
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.lse = lse;

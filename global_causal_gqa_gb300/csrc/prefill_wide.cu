@@ -547,13 +547,9 @@ int launch_wide(const void *q, const void *k_rot, const void *v, void *o, float 
         !make_map_wide(&mv, v, D, S, B * Hkv, BN) || !make_map_wide(&mo, o, D, T, B * Hq, kBM))
         return GQA_ERR_CUDA;
     constexpr int smem = wide_smem_bytes<D>();
-    static bool attr_done = false;
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(prefill_wide_kernel<D>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return GQA_ERR_CUDA;
-        attr_done = true;
-    }
+    if (ensure_smem_attr(reinterpret_cast<const void *>(prefill_wide_kernel<D>), smem) !=
+        cudaSuccess)
+        return GQA_ERR_CUDA;
     WParams p;
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.lse = lse;

@@ -19,8 +19,11 @@
  * Conventions (all entry points):
  *   - Tensors are bfloat16, dense, row-major in the layouts stated per call, in device
  *     memory, 16-byte aligned.  The caller owns every buffer, descriptor array, workspace
- *     and stream; the library allocates nothing and keeps no state except one device
- *     status word per GPU.
+ *     and stream; the library allocates nothing.  Its only device state is a status word
+ *     per GPU and the fixed 16 MiB scratch array of gqa_attn_decode_static, both
+ *     compiled into the library; on the host it remembers, per device, which kernels
+ *     have had their shared-memory limit raised (a mutex guards that record, so calls
+ *     may come from several host threads and may drive several GPUs in turn).
  *   - Every call validates its arguments on the host and returns a negative gqa_status
  *     without launching anything if they are wrong.  Otherwise it enqueues its kernels on
  *     `stream` (NULL = the legacy default stream) and returns GQA_OK without waiting.
@@ -106,7 +109,8 @@ gqa_status gqa_rope_apply(const void *x, void *y, int B, int H, int T, int d, in
  * scores, or NULL.  T <= S; query t sits at position S - T + t, key s at position s.
  * window <= 0: full causal; window > 0: keys with q_pos - k_pos < window (self included).
  * scale multiplies the dot products (e.g. 1/sqrt(d)); the table's amplitude multiplies
- * them by amp^2 on top.  table_len >= S.
+ * them by amp^2 on top.  scale must be finite and > 0 (the softmax takes each row's
+ * maximum before scaling), else GQA_ERR_INVALID_ARG.  table_len >= S.
  * Key tiles wholly outside [q_pos - window + 1, q_pos] are never loaded or multiplied.
  * k_is_rotated = 0: k holds keys before RoPE (as the PLaMo cache stores them, §4.4); they
  *   are rotated once at positions 0..S-1 into `workspace`, which must hold at least
@@ -252,8 +256,9 @@ gqa_status gqa_kv_shared_append(gqa_kv_desc *descs, int nseq, const void *q, con
  * max_len: an upper bound on R over the batch (sizes the split-KV grid); a sequence with
  * R > max_len or rope_len < R is skipped and flagged in the status word.
  * workspace: device scratch of gqa_decode_workspace_bytes(nseq, Hq, d, max_len) bytes:
- * nseq Hq nsplit (d + 2) floats of split partials, nsplit = ceil(max_len / chunk) with
- * chunk = 2048 keys when max_len > 4096 and 256 otherwise.
+ * the split partials, nseq Hq nsplit (m, l) float pairs padded to a multiple of 4 floats,
+ * then nseq Hq nsplit rows of d floats, nsplit = ceil(max_len / chunk) with chunk = 2048
+ * keys when max_len > 4096 and 256 otherwise.  scale: finite and > 0.
  * d in {128, 256, 512} (Gemma-4 local / global heads), Hq/Hkv <= 8. */
 size_t gqa_decode_workspace_bytes(int nseq, int Hq, int d, int max_len);
 gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq,

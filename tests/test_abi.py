@@ -48,6 +48,44 @@ def test_yarn_amplitude_and_sizes():
     assert gqa.gqa_rope_table_bytes(0, 10) == 0
 
 
+def test_decode_workspace_layout_keeps_partials_aligned():
+    """The decode workspace holds nseq*Hq*nsplit (m, l) float pairs, then the O partials,
+    which the kernel writes with 16-byte stores.  For odd nseq*Hq*nsplit the pairs take an
+    odd number of 8-byte slots, so the O rows would start 8 bytes off a 16-byte boundary
+    unless the pairs are padded: the bytes before the O rows (the total minus the O rows'
+    nseq*Hq*nsplit*d floats) must be a multiple of 16 and hold the pairs with at most 8
+    bytes of padding."""
+    for nseq in (1, 2, 3, 5, 31):
+        for Hq in (1, 2, 3, 5, 7, 64):
+            for d in (128, 256, 512):
+                for max_len in (1, 256, 257, 768, 1280, 4096, 4097, 6145, 65536):
+                    chunk = 2048 if max_len > 4096 else 256
+                    ns = -(-max_len // chunk)
+                    total = gqa.gqa_decode_workspace_bytes(nseq, Hq, d, max_len)
+                    head = total - nseq * Hq * ns * d * 4
+                    pairs = 2 * nseq * Hq * ns * 4
+                    assert head % 16 == 0, (nseq, Hq, d, max_len)
+                    assert pairs <= head <= pairs + 8, (nseq, Hq, d, max_len)
+
+
+def test_non_positive_scale_rejected_on_host():
+    """The kernels take each row's maximum score before scaling, which is only the
+    maximum of the scaled scores for scale > 0: every attention call rejects others."""
+    L = gqa.lib()
+    S = gqa.STATUS_NAMES
+    fake = 0x10000
+    wsb = gqa.gqa_decode_workspace_bytes(1, 2, 128, 64)
+    for bad in (0.0, -0.125, float("-inf"), float("nan")):
+        assert S[L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 2, 1, 128, 0, bad,
+                                    fake, 8, 1, None, 0, None)] == "GQA_ERR_INVALID_ARG"
+        assert S[L.gqa_attn_decode(fake, fake, 1, 2, 1, 128, bad, 64, fake, None, fake, wsb,
+                                   None)] == "GQA_ERR_INVALID_ARG"
+        assert S[L.gqa_attn_decode_kv_shared(fake, fake, 1, 2, 1, 128, bad, fake, 64, fake,
+                                             None, fake, wsb, None)] == "GQA_ERR_INVALID_ARG"
+        assert S[L.gqa_attn_decode_static(fake, fake, 1, 2, 1, 128, bad, 64, fake, None,
+                                          None)] == "GQA_ERR_INVALID_ARG"
+
+
 def test_bad_arguments_rejected_on_host():
     L = gqa.lib()
     S = gqa.STATUS_NAMES

@@ -237,3 +237,30 @@ def test_long_split_boundaries():
     assert np.array_equal(st.counts(), rcounts)
     gu.compare(o, ro, what="decode, 2048-key splits")
     gu.compare(lse, rl, what="decode lse, 2048-key splits")
+
+
+@pytest.mark.parametrize("nseq_lin,Hq,Hkv,d,max_len",
+                         [(1, 1, 1, 128, 256), (3, 3, 1, 128, 768), (1, 5, 1, 256, 256),
+                          (3, 7, 1, 128, 1280), (1, 3, 1, 512, 768), (3, 1, 1, 128, 6144)])
+def test_odd_partial_counts(nseq_lin, Hq, Hkv, d, max_len):
+    """nseq * Hq * nsplit odd: the (m, l) pairs of the workspace fill an odd number of
+    8-byte slots, and the O partials after them must still start on a 16-byte boundary
+    (they are written with 16-byte stores).  One ring per batch keeps nseq odd when a
+    linear count is even."""
+    gu.require_gpu()
+    lengths = [max_len - 1 - 97 * i for i in range(nseq_lin - 1)] + [min(40, max_len - 1)]
+    rings = [] if nseq_lin % 2 else [(64, 150)]
+    x = _random_batch(lengths, rings, Hq, Hkv, d, seed=1000 + Hq * 10 + nseq_lin)
+    if d == 512:
+        x = replace(x, rope=[PROPE if not r else LOCAL for r in x.is_ring])
+    nseq = len(lengths) + len(rings)
+    chunk = 2048 if max_len > 4096 else 256
+    assert (nseq * Hq * -(-max_len // chunk)) % 2 == 1
+    st = DecodeSetup(x, d)
+    scale = 1 / math.sqrt(d)
+    o, lse, slots = run_step(st, Hq, Hkv, scale, max_len=max_len)
+    ro, rl, rslots, rcounts = oracle_step(x, d, scale)
+    assert np.array_equal(slots.cpu().numpy().astype(np.int64), rslots)
+    assert np.array_equal(st.counts(), rcounts)
+    gu.compare(o, ro, what=f"decode nseq={nseq} Hq={Hq} d={d} max_len={max_len}")
+    gu.compare(lse, rl, what="decode lse")
