@@ -547,18 +547,13 @@ def e2e_decode(w, st, steps, warmup, stream, kv_bytes):
 # whole-model decode step (every layer of the hybrid decoder, CUDA graph)
 # ----------------------------------------------------------------------------------------
 
-def bench_decode_model(w, steps, warmup, stream, peaks, peak_src):
-    """One step = kv_append + decode for every layer (7 local ring layers then 1 global
-    linear layer per period), captured once in a CUDA graph and replayed.  Caches and
-    inputs are drawn on the device (synthetic N(0,1), seeded); every layer's descriptors
-    live in one buffer whose counts are restored by a single copy at the start of each
-    replay, so each step appends into the same slots.
-    Reported against the pages' byte model: K and V read once per (sequence, KV head),
-    4 Hkv d [n_global N + n_local min(N, W)] bytes per sequence."""
-    import numpy as np
+def decode_model_stack(w):
+    """The whole-model decode step's layers (7 local ring layers then 1 global linear
+    layer per period), with caches and inputs drawn on the device (synthetic N(0,1),
+    seeded), as a LayerStack whose descriptors live in one buffer."""
     import torch
     import global_causal_gqa_gb300 as gqa
-    from global_causal_gqa_gb300 import accounting as acc
+    from global_causal_gqa_gb300.model_step import Layer, LayerStack
     gen = torch.Generator(device="cuda").manual_seed(w.seed)
     rnd = lambda *shape: torch.randn(*shape, generator=gen, device="cuda").to(torch.bfloat16)  # noqa: E731
     tables = {}
@@ -569,40 +564,36 @@ def bench_decode_model(w, steps, warmup, stream, peaks, peak_src):
         gqa.gqa_rope_table_build(t, f, w.d, rope.amp, n)
         tables[is_g] = (t, n)
     layers = []
-    desc_rows = []
     for l in range(w.layers):
         is_g = (l % w.period) == w.period - 1
         cap = w.N if is_g else w.W
-        kc = rnd(w.nseq, w.Hkv, cap, w.d)
-        vc = rnd(w.nseq, w.Hkv, cap, w.d)
         tab, tlen = tables[is_g]
-        a = gqa.make_kv_descs([kc[i] for i in range(w.nseq)], [vc[i] for i in range(w.nseq)],
-                              [tab] * w.nseq, [cap] * w.nseq, [w.N - 1] * w.nseq,
-                              [0 if is_g else 1] * w.nseq, [tlen] * w.nseq)
-        desc_rows.append(torch.from_numpy(a.view(np.uint8).copy()))
-        layers.append({"kc": kc, "vc": vc,
-                       "q": rnd(w.nseq, w.Hq, w.d), "k_new": rnd(w.nseq, w.Hkv, w.d),
-                       "v_new": rnd(w.nseq, w.Hkv, w.d), "o": torch.empty(w.nseq, w.Hq, w.d,
-                                                                          dtype=torch.bfloat16,
-                                                                          device="cuda")})
-    descs0 = torch.stack(desc_rows).cuda()     # [layers, nseq * sizeof(gqa_kv_desc)]
-    descs = descs0.clone()
-    for l, L in enumerate(layers):
-        L["descs"] = descs[l]                   # contiguous row: this layer's array
-    max_len = w.N
-    wsb = gqa.gqa_decode_workspace_bytes(w.nseq, w.Hq, w.d, max_len)
-    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        layers.append(Layer(k_cache=rnd(w.nseq, w.Hkv, cap, w.d),
+                            v_cache=rnd(w.nseq, w.Hkv, cap, w.d),
+                            q=rnd(w.nseq, w.Hq, w.d), k_new=rnd(w.nseq, w.Hkv, w.d),
+                            v_new=rnd(w.nseq, w.Hkv, w.d),
+                            o=torch.empty(w.nseq, w.Hq, w.d, dtype=torch.bfloat16,
+                                          device="cuda"),
+                            table=tab, table_len=tlen, is_ring=not is_g,
+                            count_before=[w.N - 1] * w.nseq))
+    return LayerStack(layers, w.Hq, w.Hkv, w.d, w.scale, max_len=w.N)
+
+
+def bench_decode_model(w, steps, warmup, stream, peaks, peak_src):
+    """One step = kv_append + decode for every layer, captured once in a CUDA graph and
+    replayed; every layer's counts are restored by a single copy at the start of each
+    replay, so each step appends into the same slots.
+    Reported against the pages' byte model: K and V read once per (sequence, KV head),
+    4 Hkv d [n_global N + n_local min(N, W)] bytes per sequence."""
+    import torch
+    import global_causal_gqa_gb300 as gqa
+    from global_causal_gqa_gb300 import accounting as acc
+    stack = decode_model_stack(w)
     n_g = w.layers // w.period
     n_l = w.layers - n_g
     bytes_step = w.nseq * 2 * 2 * w.Hkv * w.d * (n_g * w.N + n_l * min(w.N, w.W))
     assert bytes_step == w.nseq * acc.kv_bytes_per_token(w.layers, w.Hkv, w.d, w.N, w.W)
-
-    def body():
-        descs.copy_(descs0, non_blocking=True)
-        for L in layers:
-            gqa.gqa_kv_append(L["descs"], w.nseq, L["k_new"], L["v_new"], w.Hkv, w.d, None)
-            gqa.gqa_attn_decode(L["q"], L["descs"], w.nseq, w.Hq, w.Hkv, w.d, w.scale, max_len,
-                                L["o"], None, ws, wsb)
+    body = stack.step
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
@@ -623,13 +614,7 @@ def bench_decode_model(w, steps, warmup, stream, peaks, peak_src):
     torch.cuda.synchronize()
     assert gqa.gqa_get_device_status() == 0
     eager_ms = timed(body, steps)
-    graph = torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(graph, stream=side):
-            body()
-    torch.cuda.current_stream().wait_stream(side)
+    graph = stack.capture()
     for _ in range(warmup):
         graph.replay()
     torch.cuda.synchronize()

@@ -25,10 +25,11 @@
 //
 // Shared K/V projection (Gemma 4 global layers, attention_k_eq_v, §5.2 and §8 of the same
 // page): the cache holds one row Zn = N_1(Z) per token; the values are Zn and the keys
-// RoPE(bf16(gamma_k) * Zn), the gain applied in bf16 to each loaded K fragment before the
-// rotation.  Each row is loaded once, in the K layout; the V fragments are the 8x8
-// transposes (movmatrix) of those registers taken before the gain and the rotation, so
-// every byte of the cache crosses L1 once: half the traffic of separate K and V.
+// RoPE(gamma_k * Zn), the fp32 gain multiplied into each loaded K element in fp32 and
+// rotated in fp32, with one rounding to bf16 for the MMA.  Each row is loaded once, in the
+// K layout; the V fragments are the 8x8 transposes (movmatrix) of those registers taken
+// before the gain and the rotation, so every byte of the cache crosses L1 once: half the
+// traffic of separate K and V.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -95,6 +96,35 @@ __device__ __forceinline__ void rotate_word(uint4 &a, uint4 &b, int q, const flo
     bw = pack_bf16x2(fmaf(a0, t.y, b0 * t.x), fmaf(a1, t.w, b1 * t.z));
 }
 
+// Shared K/V keys: multiplies the two pairs in word q of chunks a and b by the key gain in
+// fp32 (ga: a's two elements, gb: b's), rotates them by t and rounds once to bf16.
+__device__ __forceinline__ void gain_rotate_word(uint4 &a, uint4 &b, int q, const float4 &t,
+                                                 const float2 &ga, const float2 &gb) {
+    uint32_t &aw = q == 0 ? a.x : q == 1 ? a.y : q == 2 ? a.z : a.w;
+    uint32_t &bw = q == 0 ? b.x : q == 1 ? b.y : q == 2 ? b.z : b.w;
+    // packed over the word's two pairs: (a0, a1) and (b0, b1)
+    const float2 av = fmul2(make_float2(bf16lo(aw), bf16hi(aw)), ga);
+    const float2 bv = fmul2(make_float2(bf16lo(bw), bf16hi(bw)), gb);
+    const float2 c = make_float2(t.x, t.z), s = make_float2(t.y, t.w);
+    const float2 ra = fsub2(fmul2(av, c), fmul2(bv, s));
+    const float2 rb = ffma2v(av, s, fmul2(bv, c));
+    aw = pack_bf16x2(ra.x, ra.y);
+    bw = pack_bf16x2(rb.x, rb.y);
+}
+
+// The same for pairs that never rotate (p-RoPE): the gain alone, one rounding.
+__device__ __forceinline__ void gain_word(uint4 &a, int q, const float2 &g) {
+    uint32_t &aw = q == 0 ? a.x : q == 1 ? a.y : q == 2 ? a.z : a.w;
+    const float2 v = fmul2(make_float2(bf16lo(aw), bf16hi(aw)), g);
+    aw = pack_bf16x2(v.x, v.y);
+}
+
+// Gain pair qq (elements 2 qq, 2 qq + 1) of a chunk whose 8 gains are g[0], g[1].
+__device__ __forceinline__ float2 gain_pair(const float4 (&g)[2], int qq) {
+    const float4 &h = g[qq >> 1];
+    return (qq & 1) ? make_float2(h.z, h.w) : make_float2(h.x, h.y);
+}
+
 // Rotates the 8 pairs (a[e], b[e]) held in two 16-byte chunks by the table entries
 // starting at `tab` (8 consecutive float2 = (amp cos, amp sin)).
 __device__ __forceinline__ void rotate8(uint4 &a, uint4 &b, const float2 *tab) {
@@ -137,13 +167,8 @@ __device__ __forceinline__ SeqView seq_view(const gqa_kv_desc &desc, int max_len
     return v;
 }
 
-// Shared memory after the table stages and the exchange: the key gain as bf16 pairs.
-constexpr int kDecodeSmemShared = kDecodeSmem + kMaxHeadDim * 2;
-
-__device__ __forceinline__ uint4 mul_bf16x8(const uint4 &a, const uint4 &b) {
-    return make_uint4(mul_bf16x2(a.x, b.x), mul_bf16x2(a.y, b.y), mul_bf16x2(a.z, b.z),
-                      mul_bf16x2(a.w, b.w));
-}
+// Shared memory after the table stages and the exchange: the key gain, fp32 [d].
+constexpr int kDecodeSmemShared = kDecodeSmem + kMaxHeadDim * 4;
 
 template <int PARTS, bool SHARED>   // warps per KV head: d = 128 PARTS; shared K/V rows
 __global__ void __launch_bounds__(kWarps * 32, 1)
@@ -156,11 +181,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     griddep_wait();               // the appended token, counts and partials of earlier kernels
     griddep_launch_dependents();  // the combine kernel may start launching
     extern __shared__ float4 dsmem[];
-    uint4 *sgain = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(dsmem) + kDecodeSmem);
+    // the key gain as float pairs: entry i holds elements 2i, 2i + 1
+    float2 *sgain = reinterpret_cast<float2 *>(reinterpret_cast<uint8_t *>(dsmem) + kDecodeSmem);
     if constexpr (SHARED) {
         // before any warp may leave: every thread takes part in the barrier
         for (int i = threadIdx.x; i < d / 2; i += blockDim.x)
-            reinterpret_cast<uint32_t *>(sgain)[i] = pack_bf16x2(k_gamma[2 * i], k_gamma[2 * i + 1]);
+            sgain[i] = reinterpret_cast<const float2 *>(k_gamma)[i];
         __syncthreads();
     }
     const int split = blockIdx.x, seq = blockIdx.y;
@@ -366,24 +392,44 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                     vt0[c][qq] = transpose8x8(word(bl.k0[c], qq));
                     vt1[c][qq] = transpose8x8(word(bl.k1[c], qq));
                 }
-            // keys = bf16(gamma_k) * Zn before the rotation; chunk lc holds elements
-            // 8 gchunk(lc) .. + 7 in order, as does word group gchunk(lc) of the gain
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint4 gw = sgain[gchunk(4 * c + tq)];
-                bl.k0[c] = mul_bf16x8(bl.k0[c], gw);
-                bl.k1[c] = mul_bf16x8(bl.k1[c], gw);
-            }
         }
-        // rotate K at logical positions kb + gq, kb + gq + 8 (clamped rows: k_end - 1)
+        // rotate K at logical positions kb + gq, kb + gq + 8 (clamped rows: k_end - 1).
+        // Shared rows: keys = gamma_k * Zn, formed in fp32 inside the rotation; word qq of
+        // chunk lc holds elements 8 gchunk(lc) + 2 qq, + 1, gain pair 4 gchunk(lc) + qq.
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
+            // the 8 gains of chunks c and c + 2 (shared rows only)
+            float4 gA[2], gB[2];
+            if constexpr (SHARED) {
+                const float4 *sg4 = reinterpret_cast<const float4 *>(sgain);
+                gA[0] = sg4[2 * gchunk(4 * c + tq)];
+                gA[1] = sg4[2 * gchunk(4 * c + tq) + 1];
+                gB[0] = sg4[2 * gchunk(4 * (c + 2) + tq)];
+                gB[1] = sg4[2 * gchunk(4 * (c + 2) + tq) + 1];
+            }
             if (c == 0 ? rot0 : rot1) {
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
                     const int sw = lane ^ (qq << 1);
-                    rotate_word(bl.k0[c], bl.k0[c + 2], qq, stg[(4 * c + qq) * 32 + sw]);
-                    rotate_word(bl.k1[c], bl.k1[c + 2], qq, stg[(8 + 4 * c + qq) * 32 + sw]);
+                    const float4 t0 = stg[(4 * c + qq) * 32 + sw];
+                    const float4 t1 = stg[(8 + 4 * c + qq) * 32 + sw];
+                    if constexpr (SHARED) {
+                        const float2 ga = gain_pair(gA, qq), gb = gain_pair(gB, qq);
+                        gain_rotate_word(bl.k0[c], bl.k0[c + 2], qq, t0, ga, gb);
+                        gain_rotate_word(bl.k1[c], bl.k1[c + 2], qq, t1, ga, gb);
+                    } else {
+                        rotate_word(bl.k0[c], bl.k0[c + 2], qq, t0);
+                        rotate_word(bl.k1[c], bl.k1[c + 2], qq, t1);
+                    }
+                }
+            } else if constexpr (SHARED) {
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const float2 ga = gain_pair(gA, qq), gb = gain_pair(gB, qq);
+                    gain_word(bl.k0[c], qq, ga);
+                    gain_word(bl.k0[c + 2], qq, gb);
+                    gain_word(bl.k1[c], qq, ga);
+                    gain_word(bl.k1[c + 2], qq, gb);
                 }
             }
         }

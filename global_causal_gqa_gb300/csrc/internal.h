@@ -77,7 +77,7 @@ __host__ __device__ inline size_t decode_ml_floats(int nseq, int Hq, int nsplit)
 // drives needs its own call.  Thread-safe.
 cudaError_t ensure_smem_attr(const void *func, int bytes);
 // k_gamma == nullptr: separate K and V caches; otherwise each desc.k holds Zn of a shared
-// K/V projection (keys RoPE(bf16(gamma_k) * Zn), values Zn) and desc.v is not read
+// K/V projection (keys RoPE(gamma_k * Zn) formed in fp32, values Zn) and desc.v is not read
 cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
                           int d, float scale, int max_len, void *o, float *lse,
                           float *ws, int *status, cudaStream_t s,

@@ -374,6 +374,17 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
     return r;
 }
 
+// Packed fp32x2 a * b, round to nearest (sm_100+).
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
 // Packed fp32x2 a * b + c, all operands pairs, round to nearest (sm_100+).
 __device__ __forceinline__ float2 ffma2v(float2 a, float2 b, float2 c) {
     float2 r;
@@ -412,13 +423,6 @@ __device__ __forceinline__ float2 ex2_fma2(float2 x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// Two bf16 products, each rounded once to nearest-even from the exact product.
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 

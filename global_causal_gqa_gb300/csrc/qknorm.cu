@@ -12,10 +12,9 @@
 // Shared K/V projection (Gemma 4 global layers, attention_k_eq_v, §5.2 and §8): one
 // projection output Z gives K = RoPE(N_{gamma_k}(Z)) and V = N_1(Z).  The cache stores
 // only Zn = bf16(N_1(Z)); since N_gamma(Z) = gamma * N_1(Z), the keys are recomputed from
-// it as RoPE(bf16(bf16(gamma_k) * Zn)) -- the gain applied in bf16 to the stored row,
-// exactly as the decode kernel applies it -- so prefill and decode rotate the same bf16
-// keys (the rotation's two products may round in a different order: at most one bf16
-// step apart).
+// it as RoPE(gamma_k * Zn): the fp32 gain times the stored bf16 row, rotated in fp32 and
+// rounded once to bf16, as the decode kernel forms them (the rotation's products may round
+// in a different order there: at most one bf16 step apart).
 //
 // One warp per row.  Lane l holds the 32-bit words (bf16 pairs) l, l + 32, ... of the
 // row's first half and the words d/4 later of the second half, so each RoPE pair
@@ -93,7 +92,8 @@ __device__ __forceinline__ void finish_row(const Row &row, int d, int lane, floa
 }
 
 // Shared K/V row: Zn = bf16(x * inv) to `v_out` (nullable); the key row
-// RoPE(bf16(bf16(gamma) * Zn)) by the table row `tab` to `k_rot` (nullable).
+// RoPE(gamma * Zn), formed in fp32 from the rounded Zn and rounded once, by the table row
+// `tab` to `k_rot` (nullable).
 __device__ __forceinline__ void finish_row_shared(const Row &row, int d, int lane, float inv,
                                                   const float *gamma, uint32_t *v_out,
                                                   uint32_t *k_rot, const float2 *tab) {
@@ -110,9 +110,8 @@ __device__ __forceinline__ void finish_row_shared(const Row &row, int d, int lan
             }
             if (k_rot) {
                 const float2 ga = gain2(gamma, w), gb = gain2(gamma, w + hw);
-                const uint32_t ka = mul_bf16x2(za, pack_bf16x2(ga.x, ga.y));
-                const uint32_t kb = mul_bf16x2(zb, pack_bf16x2(gb.x, gb.y));
-                const float a0 = bf16lo(ka), a1 = bf16hi(ka), b0 = bf16lo(kb), b1 = bf16hi(kb);
+                const float a0 = bf16lo(za) * ga.x, a1 = bf16hi(za) * ga.y;
+                const float b0 = bf16lo(zb) * gb.x, b1 = bf16hi(zb) * gb.y;
                 const float4 t = reinterpret_cast<const float4 *>(tab)[w];
                 k_rot[w] = pack_bf16x2(a0 * t.x - b0 * t.y, a1 * t.z - b1 * t.w);
                 k_rot[w + hw] = pack_bf16x2(a0 * t.y + b0 * t.x, a1 * t.w + b1 * t.z);

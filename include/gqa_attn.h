@@ -217,15 +217,16 @@ gqa_status gqa_qk_norm_append(gqa_kv_desc *descs, int nseq, const void *q, const
  * output Z [.., Hkv, .., d] per token gives both K = RoPE(N_{gamma_k}(Z)) and V = N_1(Z),
  * N_1 being RMSNorm without a gain (eps as above).  Such a layer needs to cache only
  * Zn = N_1(Z): since N_gamma(Z) = gamma * N_1(Z), the keys are recomputed from it.  The
- * library does exactly that, in bf16: the stored row is Zn rounded once to bf16, and the
- * key is RoPE(bf16(bf16(gamma_k) * Zn)) -- the gain rounded to bf16 and multiplied into
- * the stored row with one rounding -- in prefill and decode alike.  Gains are device fp32
+ * library does exactly that: the stored row is Zn rounded once to bf16, and the key is
+ * RoPE(gamma_k * Zn) -- the fp32 gain times the stored row, rotated in fp32 and rounded
+ * once to bf16 -- in prefill and decode alike (the two may round the rotation's products
+ * in a different order, at most one bf16 step apart).  Gains are device fp32
  * [d], 16-byte aligned, one per layer, shared by every head; d in {64, 128, 256, 512}
  * (decode: {128, 256, 512}).
  *
  * gqa_qk_norm_rope_kv_shared (prefill form): q [B, Hq, T, d] -> q_out = N_{q_gamma}(q)
  * (rotated later, inside gqa_attn_prefill); z [B, Hkv, T, d] -> v_out = Zn (the values,
- * and what the cache stores; nullable) and k_rot = RoPE(bf16(gamma_k) * Zn) at positions
+ * and what the cache stores; nullable) and k_rot = RoPE(gamma_k * Zn) at positions
  * pos0 + t (nullable; pass it to gqa_attn_prefill with k_is_rotated = 1 and v_out as v).
  * q, q_out and q_gamma may all be NULL (then Hq is ignored) to process Z alone; at least
  * one of v_out, k_rot must be given; k_gamma and the table are needed only for k_rot.
@@ -236,7 +237,7 @@ gqa_status gqa_qk_norm_append(gqa_kv_desc *descs, int nseq, const void *q, const
  * count update, slots_out and GQA_ERR_CAPACITY of gqa_kv_append; desc.v is not written.
  *
  * gqa_attn_decode_kv_shared: as gqa_attn_decode (same arguments, workspace and results),
- * over caches of Zn at desc.k: keys RoPE(bf16(k_gamma) * Zn) at positions 0..R-1, values
+ * over caches of Zn at desc.k: keys RoPE(k_gamma * Zn) at positions 0..R-1, values
  * Zn; desc.v is not read.  The cache rows are read once from memory for both roles, half
  * the bytes of separate K and V caches. */
 gqa_status gqa_qk_norm_rope_kv_shared(const void *q, const void *z, void *q_out, void *v_out,

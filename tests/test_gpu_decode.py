@@ -264,3 +264,37 @@ def test_odd_partial_counts(nseq_lin, Hq, Hkv, d, max_len):
     assert np.array_equal(st.counts(), rcounts)
     gu.compare(o, ro, what=f"decode nseq={nseq} Hq={Hq} d={d} max_len={max_len}")
     gu.compare(lse, rl, what="decode lse")
+
+
+@pytest.mark.parametrize("name", ["gemma4_decode_global", "gemma4_decode_local"])
+def test_gemma4_decode_batch_full_size(name):
+    """The benchmark's Gemma-4-shaped decode batches in the launch the benchmark times:
+    32 linear caches of 8192..65536 tokens at d = 512 (2 KV heads, p-RoPE), and 32 rings
+    of 1024 at d = 256 (8 KV heads).  Every slot and count is checked bit for bit; the
+    outputs of every ring, and of the longest, the shortest and 4 seeded linear caches,
+    are compared with the oracle."""
+    gu.require_gpu()
+    w = WORKLOADS[name]
+    x = decode_inputs(w)
+    st = DecodeSetup(x, w.d)
+    max_len = max(w.global_len_range[1], w.window)
+    o, lse, slots = run_step(st, w.Hq, w.Hkv, w.scale, max_len)
+    orc = gu.orc()
+    want_slots = [orc.append_slot(r, c, cap) for r, c, cap in zip(x.is_ring, x.count_before,
+                                                                    x.cap)]
+    assert slots.cpu().tolist() == want_slots
+    assert st.counts().tolist() == [c + 1 for c in x.count_before]
+    if w.n_global:
+        lens = np.array(x.count_before)
+        rng = np.random.default_rng(12)
+        idx = sorted({int(lens.argmax()), int(lens.argmin())} |
+                     set(rng.choice(w.nseq, 4, replace=False).tolist()))
+    else:
+        idx = list(range(w.nseq))
+    sub = lambda a: [a[i] for i in idx]  # noqa: E731
+    xs = DecodeInputs(x.q[idx], x.k_new[idx], x.v_new[idx], sub(x.k_cache), sub(x.v_cache),
+                      sub(x.cap), sub(x.count_before), sub(x.is_ring), sub(x.rope))
+    ro, rl, rslots, _ = oracle_step(xs, w.d, w.scale)
+    assert rslots.tolist() == [want_slots[i] for i in idx]
+    gu.compare(o[idx], ro, what=f"{name} ({len(idx)} sequences)")
+    gu.compare(lse[idx], rl, what=f"{name} lse")

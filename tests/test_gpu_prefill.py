@@ -140,14 +140,13 @@ def test_wide_head_edge_cases(layer):
     _full_case(layer)
 
 
-def test_gemma4_local_layer_full_size_sampled():
-    """T=S=16384, 16 query / 8 KV heads, d=256, window 1024 (layer 0 of the period)."""
-    _sampled_case(WORKLOADS["gemma4_period_6layer"].layers[0], 2048, 4)
-
-
-def test_gemma4_global_layer_full_size_sampled():
-    """T=S=16384, 16 query / 2 KV heads, d=512, full causal, partial RoPE (layer 5)."""
-    _sampled_case(WORKLOADS["gemma4_period_6layer"].layers[5], 1024, 5)
+@pytest.mark.parametrize("index", range(6))
+def test_gemma4_period_layer_full_size_sampled(index):
+    """Every layer of the Gemma-4-shaped period at full size (T=S=16384, 16 query heads):
+    layers 0-4 d=256, 8 KV heads, window 1024; layer 5 d=512, 2 KV heads, full causal,
+    partial RoPE.  4096 sampled rows per layer, covering every head of two KV groups and
+    the window, tile and sequence edges."""
+    _sampled_case(WORKLOADS["gemma4_period_6layer"].layers[index], 4096, 40 + index)
 
 
 @pytest.mark.parametrize("name,index", [("plamo3_local_prefill", 0),
