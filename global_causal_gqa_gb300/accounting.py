@@ -85,4 +85,6 @@ def prefill_kernel_name(d: int, T: int, S: int, window: int) -> str:
     """The prefill kernel the library launches for head dim d at these positions."""
     if d == 128:
         return prefill_d128_kernel(T, S, window)
+    if d == 512:
+        return "prefill_pair_kernel"
     return f"prefill_wide_kernel<{d}>"

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgqa_attn.so")
 SOURCES = ["api.cu", "rope.cu", "kv.cu", "decode.cu", "prefill.cu", "prefill_stream.cu",
-           "prefill_wide.cu", "qknorm.cu", "chunk.cu", "watchdog.cu"]
+           "prefill_wide.cu", "prefill_pair.cu", "qknorm.cu", "chunk.cu", "watchdog.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",

@@ -99,6 +99,11 @@ int launch_prefill_wide(const void *q, const void *k_rot, const void *v, void *o
                         int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
                         const float *table, int *status, cudaStream_t s);
 
+// Prefill for d = 512 on a cluster of two CTAs (prefill_pair.cu); returns a gqa_status
+int launch_prefill_pair(const void *q, const void *k_rot, const void *v, void *o, float *lse,
+                        int B, int T, int S, int Hq, int Hkv, int window, float scale,
+                        const float *table, int *status, cudaStream_t s);
+
 // Chunked prefill over a cache (chunk.cu)
 cudaError_t launch_prefill_gather(const gqa_kv_desc *desc, const void *k_new, const void *v_new,
                                   int T, int Hkv, int d, void *k_out, void *v_out, int S,

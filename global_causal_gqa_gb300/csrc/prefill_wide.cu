@@ -1,22 +1,20 @@
-// prefill_wide.cu -- causal / sliding-window GQA prefill for wide heads (d = 256, 512) on
-// tcgen05 tensor cores.
+// prefill_wide.cu -- causal / sliding-window GQA prefill for d = 256 heads on tcgen05
+// tensor cores (d = 512 runs on a pair of CTAs, prefill_pair.cu).
 //
 // Same computation as prefill.cu ("PLaMo 3アーキテクチャ徹底解析" §4.5, §5.1; the
-// Gemma-4 shapes of the qiita.com Gemma-4-26B-A4B explainer, Attention block section, and
-// the p-RoPE of §6.4), for heads too wide for two query tiles to share tensor memory:
-// a 128 x d fp32 output tile alone takes d of the 512 TMEM columns.
+// Gemma-4 local layers of the qiita.com Gemma-4-26B-A4B explainer, Attention block
+// section), for heads too wide for two query tiles to share tensor memory: a 128 x 256
+// fp32 output tile takes half of the 512 TMEM columns.
 //
-// CTA = (batch, query head, 128-row query block, output slice).  One query tile per CTA;
+// CTA = (batch, query head, 128-row query block).  One query tile per CTA;
 // its score tile S (128 keys) is double-buffered in TMEM so that S(j+2) = Q K(j+2)^T can
 // run on the tensor core while the softmax warps work on S(j+1).  TMEM: S_a, S_b (128
 // columns each) and O (the CTA's 256 output columns).  K (128-dim chunks of a key tile)
 // and V (128-dim halves of the CTA's output columns) stream through one ring of 32 KB
 // slots, loaded by TMA (128-byte swizzle) in exactly the order the MMA thread uses them:
-// K(0), K(1), then V(j), K(j + 2) for j = 0, 1, ...
-//   d = 256: one output slice; Q 64 KB + 5 ring slots.
-//   d = 512: two output slices per query tile: both CTAs of a pair compute the full S
-//            (the score contraction runs over all 512 dims) and each accumulates half of
-//            O; Q 128 KB + 3 ring slots.
+// K(0), K(1), then V(j), K(j + 2) for j = 0, 1, ...; Q 64 KB + 5 ring slots.
+// (The kernel is written for a head of D dims with DV output columns per CTA; it is
+// instantiated for D = DV = 256 only.)
 // Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2-3 idle, 4-7 softmax/epilogue (one
 // thread per query row).  Q is rotated (RoPE) in shared memory after it lands, by all 8
 // warps, while the first K tiles load; pairs (j, j + d/2) sit at the same offset of boxes
@@ -43,10 +41,6 @@ struct Wide;
 template <>
 struct Wide<256> {
     static constexpr int BN = 128, DV = 256, NS = 5;
-};
-template <>
-struct Wide<512> {
-    static constexpr int BN = 128, DV = 256, NS = 3;
 };
 constexpr int kSlotBytes = 128 * 256;   // 128 rows x 128 bf16 (two 64-column TMA boxes)
 constexpr int kMaxSlots = 5;
@@ -574,12 +568,14 @@ int launch_wide(const void *q, const void *k_rot, const void *v, void *o, float 
 int launch_prefill_wide(const void *q, const void *k_rot, const void *v, void *o, float *lse,
                         int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
                         const float *table, int *status, cudaStream_t s) {
+    // d = 512: a 128 x 512 fp32 output tile fills TMEM, so a pair of CTAs splits the
+    // score and output roles (prefill_pair.cu)
     if (d == 256)
         return launch_wide<256>(q, k_rot, v, o, lse, B, T, S, Hq, Hkv, window, scale, table,
                                 status, s);
     if (d == 512)
-        return launch_wide<512>(q, k_rot, v, o, lse, B, T, S, Hq, Hkv, window, scale, table,
-                                status, s);
+        return launch_prefill_pair(q, k_rot, v, o, lse, B, T, S, Hq, Hkv, window, scale, table,
+                                   status, s);
     return GQA_ERR_UNSUPPORTED;
 }
 

@@ -31,7 +31,13 @@ __device__ __forceinline__ void set_status(int *status, int code) {
 
 // Diagnostic code of the first bounded wait that expired, stored next to the status word:
 // (kernel << 24) | (role << 20) | (barrier << 16) | (tile index & 0xffff).
-enum DiagKernel { kDiagPrefill = 1, kDiagPrefillWide = 2, kDiagDecode = 3, kDiagWatchdog = 4 };
+enum DiagKernel {
+    kDiagPrefill = 1,
+    kDiagPrefillWide = 2,
+    kDiagDecode = 3,
+    kDiagWatchdog = 4,
+    kDiagPrefillPair = 5
+};
 __device__ __forceinline__ void set_timeout(int *status, int kernel, int role, int barrier,
                                             int tile) {
     if (!status) return;
@@ -321,6 +327,69 @@ __device__ __forceinline__ void griddep_wait() {
 }
 __device__ __forceinline__ void griddep_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- thread-block clusters (distributed shared memory) ------------------------------------
+// This CTA's rank in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of the variable at shared::cta address `addr` in the CTA of
+// the cluster with rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Every thread of every CTA of the cluster arrives, then waits for all of them (release /
+// acquire at cluster scope).  Every thread of the cluster must execute it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// 1-D bulk copy from this CTA's shared memory to the shared memory of a CTA of the cluster
+// (dst and bar are shared::cluster addresses in that CTA); completes `bytes` of
+// transaction on that CTA's mbarrier.  Addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_s2c(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst),
+        "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Arrives once on an mbarrier of another CTA of the cluster (shared::cluster address),
+// ordering this thread's earlier memory accesses before the arrival at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// mbar_wait for a phase completed from another CTA of the cluster (acquire at cluster
+// scope): an arrival or a transaction count from a remote thread or copy.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > GQA_WAIT_LIMIT_NS) return false;
+    }
 }
 
 // ---- misc ----------------------------------------------------------------------------------

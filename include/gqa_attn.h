@@ -300,7 +300,8 @@ gqa_status gqa_get_device_status(gqa_stream_t stream);
  * device-side bounded waits that expired since the last call (0 where none): diag[0] the
  * first overall, diag[1..4] the first of each kernel role 0..3.  A code is
  * (kernel << 24) | (role << 20) | (barrier << 16) | (tile index & 0xffff), kernel 1 =
- * prefill d=128, 2 = prefill d=256/512, 3 = decode, 4 = gqa_watchdog_selftest.  For
+ * prefill d=128, 2 = prefill d=256, 3 = decode, 4 = gqa_watchdog_selftest,
+ * 5 = prefill d=512 (a pair of CTAs).  For
  * diagnosing GQA_ERR_DEVICE_TIMEOUT; gqa_get_device_status leaves the codes in place. */
 gqa_status gqa_get_device_diag(gqa_stream_t stream, int32_t *diag, int n);
 
