@@ -6,23 +6,27 @@
 // §6.4).  A 128 x 512 fp32 output tile fills all 512 TMEM columns of an SM, so one CTA
 // cannot hold it next to a score tile.  The pair splits the work by role:
 //   S-CTA (cluster rank 0): the rotated Q tile lives in its TMEM (bf16, 256 columns) as the
-//     A operand of S = Q K^T; K streams through a ring of 32 KB slots (128 keys x 128
+//     A operand of S = Q K^T; K streams through a 5-slot ring of 32 KB (128 keys x 128
 //     dims); S is double-buffered in TMEM (2 x 128 columns).  Its softmax warps turn S(j)
-//     into P(j) (bf16, 128 x 128) plus one rescale factor per row, store them in a local
-//     staging buffer in the layout the tensor core reads, and one bulk copy carries the
-//     packet into the O-CTA's shared memory.  It owns the running max and sum (and writes
-//     the log-sum-exp); at the end it sends the row sums.
-//   O-CTA (cluster rank 1): the whole 128 x 512 fp32 O in TMEM; V streams through the same
-//     kind of ring; O += P(j) V(j) with both operands in shared memory.  Four warps apply
-//     the rare lazy rescale of O rows before a PV product and write O / l at the end.
-// Per key tile each CTA issues 32 MMAs of 128 x 128 x 16 (S over the 512 dims; PV over
-// the 512 output dims), so the pair executes exactly the counted tensor work, where two
-// CTAs that each own half of O would both have to compute the whole score tile.
+//     into P(j) (bf16, 128 x 128) plus one rescale factor per row, store them in one of two
+//     local staging buffers in the layout the tensor core reads, and one bulk copy carries
+//     the packet into one of the O-CTA's three receive buffers.  It owns the running max
+//     and sum (and writes the log-sum-exp); at the end it sends the row sums.
+//   O-CTA (cluster rank 1): the whole 128 x 512 fp32 O in TMEM; V streams through a 4-slot
+//     ring of 32 KB (64 keys x 256 dims); O += P(j) V(j) with both operands in shared
+//     memory, 256 output columns per MMA so that each P element is read once per 256
+//     dims.  Four warps apply the rare lazy rescale of O rows before a PV product and
+//     write O / l at the end.
+// Per key tile each CTA issues the same tensor work (S: 32 MMAs of 128 x 128 x 16 over the
+// 512 dims; PV: 16 of 128 x 256 x 16), so the pair executes exactly the counted work,
+// where two CTAs that each own half of O would both compute the whole score tile.
 //
-// Packets go through two buffers on each side.  The O-CTA's warp 2 forwards "PV(j) has
-// finished" to the S-CTA (a remote mbarrier arrival); only then may P(j + 2) overwrite
-// the S-CTA's staging buffer (the copy out of it has completed, since the O-CTA saw it
-// land) and the O-CTA's receive buffer (no MMA reads it any more).
+// Two acknowledgements flow back to the S-CTA as remote mbarrier arrivals: "packet j
+// received" (the O-CTA's warp 3, as soon as the copy has landed: staging buffer j & 1 is
+// free for P(j + 2)) and "PV(j) finished" (the O-CTA's warp 2, forwarding the tensor
+// core's completion: receive buffer j % 3 is free for packet j + 3).  Three receive
+// buffers keep the loop packet -> PV -> acknowledgement -> next packet off the tensor
+// pipe's critical path.
 // Every wait is bounded; both CTAs meet at a cluster barrier before either exits, so no
 // copy or remote arrival targets the shared memory of a CTA that has finished.
 #include <cuda.h>
@@ -40,46 +44,56 @@ constexpr int kD = 512;
 constexpr int kBM = 128;                  // query rows per pair
 constexpr int kBN = 128;                  // keys per tile
 constexpr int kThreads = 256;
-constexpr int kNS = 5;                    // ring slots
+constexpr int kNS_S = 5;                  // S-CTA ring slots
+constexpr int kNS_O = 4;                  // O-CTA ring slots
 constexpr int kBox = 128 * 128;           // 128 rows x 64 bf16 (one 128-byte-swizzled TMA box)
-constexpr int kSlot = 2 * kBox;           // 128 rows x 128 bf16
-constexpr int kChunks = kD / 128;         // 128-dim chunks per key tile (K or V)
+constexpr int kVBox = 64 * 128;           // 64 keys x 64 bf16
+constexpr int kSlot = 2 * kBox;           // 32 KB: K 128 keys x 128 dims, V 64 keys x 256 dims
+constexpr int kChunks = 4;                // ring loads per key tile (K or V)
 constexpr int kPBytes = kBM * kBN * 2;    // P tile, bf16
-constexpr int kFBytes = kBM * 4;          // rescale factors, fp32
+constexpr int kFBytes = kBM * 4;          // rescale factors (or the final row sums), fp32
+constexpr int kNR = 3;                    // O-CTA receive buffers
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
-// shared memory (same layout in both CTAs: the remote addresses are local offsets)
-constexpr int OFF_RING = 0;
-constexpr int OFF_P = OFF_RING + kNS * kSlot;   // 2 P buffers (staging / receive)
-constexpr int OFF_F = OFF_P + 2 * kPBytes;      // 2 rescale-factor vectors
-constexpr int OFF_L = OFF_F + 2 * kFBytes;      // the final row sums
-constexpr int OFF_BAR = OFF_L + kFBytes;
-constexpr int kSmemBytes = OFF_BAR + 256 + 1024;
-static_assert(OFF_P % 1024 == 0 && kPBytes % 1024 == 0, "P boxes are 1024-byte aligned");
+// shared memory of the S-CTA: ring, 2 staging buffers (P, f), the row sums
+constexpr int S_OFF_P = kNS_S * kSlot;
+constexpr int S_OFF_F = S_OFF_P + 2 * kPBytes;
+constexpr int S_OFF_L = S_OFF_F + 2 * kFBytes;
+// shared memory of the O-CTA: ring, 3 receive buffers (P, f; the row sums land in the f
+// slot of the buffer after the last packet)
+constexpr int O_OFF_P = kNS_O * kSlot;
+constexpr int O_OFF_F = O_OFF_P + kNR * kPBytes;
+// the barrier block sits at the same offset in both
+constexpr int OFF_BAR = 230912;
+constexpr int kBarBytes = 320;
+constexpr int kSmemBytes = OFF_BAR + kBarBytes + 1024;
+static_assert(S_OFF_L + kFBytes <= OFF_BAR && O_OFF_F + kNR * kFBytes <= OFF_BAR, "layout");
+static_assert(S_OFF_P % 1024 == 0 && O_OFF_P % 1024 == 0 && kPBytes % 1024 == 0,
+              "P boxes are 1024-byte aligned");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // TMEM columns: S-CTA Q (bf16 pairs) and two score buffers; O-CTA all of O
 constexpr uint32_t TQ = 0, TS0 = 256, TS1 = 384, TO = 0;
 
 struct PBars {
-    uint64_t full[kNS], empty[kNS];   // ring (both)
+    uint64_t full[kNS_S], empty[kNS_S];   // ring (both; the O-CTA uses kNS_O)
     uint64_t q_rot;                   // S: Q rotated in shared memory (256 arrivals)
     uint64_t q_ready;                 // S: Q in TMEM (128)
     uint64_t s_full[2], s_free[2];    // S: score buffer written / read out (128)
     uint64_t p_staged[2];             // S: packet j stored in staging buffer j & 1 (128)
-    uint64_t pfree[2];                // S: PV of the buffer's last packet done (remote)
+    uint64_t rack[2];                 // S: packet j landed in the O-CTA (remote)
+    uint64_t pfree[kNR];              // S: PV(j) of receive buffer j % 3 done (remote)
     uint64_t l_staged;                // S: row sums stored (128)
-    uint64_t p_full[2];               // O: packet landed (transaction bytes)
-    uint64_t l_full;                  // O: row sums landed
-    uint64_t o_ok[2];                 // O: rows rescaled (or not needed) for packet j (128)
-    uint64_t pv_done[2];              // O: PV(j) complete
+    uint64_t p_full[kNR];             // O: packet (or the row sums) landed (transaction bytes)
+    uint64_t o_ok[kNR];               // O: rows rescaled (or not needed) for packet j (128)
+    uint64_t pv_done[kNR];            // O: PV(j) complete
     uint64_t o_final;                 // O: last PV complete
     uint64_t staged;                  // O: output rows staged for the TMA store (128)
     uint64_t mma_done;
     uint32_t tmem_base;
 };
-static_assert(sizeof(PBars) <= 256, "barrier block");
+static_assert(sizeof(PBars) <= kBarBytes, "barrier block");
 
 struct PairParams {
     float *lse;
@@ -106,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     PBars *bars = reinterpret_cast<PBars *>(smem + OFF_BAR);
-    uint8_t *ring = smem + OFF_RING;
+    uint8_t *ring = smem;   // the ring starts the layout in both CTAs
     const uint32_t rank = cluster_ctarank();
     const bool is_s = rank == 0;
 
@@ -121,12 +135,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q_hi = min(q_lo + kBM - 1, p.S - 1);
     const int kt_first = p.window > 0 ? max(0, q_lo - p.window + 1) / kBN : 0;
     const int n_tiles = q_hi / kBN - kt_first + 1;
-    // S-CTA: Q (4 slot loads), then K(0) chunks 0..3, K(1) ...; O-CTA: V(0) chunks 0..3, ...
+    // S-CTA: Q (4 slot loads), then K(0) chunks 0..3, K(1) ...; O-CTA: V(0) as (dims 0-255,
+    // keys 0-63), (0-255, 64-127), (256-511, 0-63), (256-511, 64-127), V(1) ...
+    const int kNS = is_s ? kNS_S : kNS_O;
     const int n_q = is_s ? 4 : 0;
     const int n_loads = n_q + kChunks * n_tiles;
+    // bytes landing on the O-CTA's p_full phase i: packet i, then the row sums as "packet" n
+    auto rx_bytes = [&](int i) {
+        return i < n_tiles ? kPBytes + kFBytes : (i == n_tiles ? kFBytes : 0);
+    };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNS; ++i) {
+        for (int i = 0; i < kNS_S; ++i) {
             mbar_init(&bars->full[i], 1);
             mbar_init(&bars->empty[i], 1);
         }
@@ -136,21 +156,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->s_free[i], 128);
             mbar_init(&bars->p_staged[i], 128);
+            mbar_init(&bars->rack[i], 1);
+        }
+        for (int i = 0; i < kNR; ++i) {
             mbar_init(&bars->pfree[i], 1);
             mbar_init(&bars->p_full[i], 1);
             mbar_init(&bars->o_ok[i], 128);
             mbar_init(&bars->pv_done[i], 1);
         }
         mbar_init(&bars->l_staged, 128);
-        mbar_init(&bars->l_full, 1);
         mbar_init(&bars->o_final, 1);
         mbar_init(&bars->staged, 128);
         mbar_init(&bars->mma_done, 1);
         if (!is_s) {
-            // the packets of tiles 0 and 1 and the row sums, before the S-CTA may send any
-            for (int i = 0; i < 2 && i < n_tiles; ++i)
-                mbar_arrive_expect_tx(&bars->p_full[i], kPBytes + kFBytes);
-            mbar_arrive_expect_tx(&bars->l_full, kFBytes);
+            // the first three receptions, before the S-CTA may send anything
+            for (int i = 0; i < kNR; ++i)
+                if (rx_bytes(i)) mbar_arrive_expect_tx(&bars->p_full[i], rx_bytes(i));
         }
         fence_mbar_init();
     }
@@ -180,12 +201,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             c0 = 128 * pu;
             c1 = mb * kBM;
             c2 = b * p.Hq + h;
-        } else {
+        } else if (is_s) {
             const int v = pu - n_q;
-            map = is_s ? &tmK : &tmV;
+            map = &tmK;
             c0 = 128 * (v % kChunks);
             c1 = (kt_first + v / kChunks) * kBN;
             c2 = b * p.Hkv + g;
+        } else {
+            // four 64 x 64 boxes: dims 256 dh + 64 i, keys 64 kh .. 64 kh + 63
+            const int w = pu % kChunks;
+            uint8_t *dst = ring + st * kSlot;
+            const int d0 = 256 * (w >> 1), r0 = (kt_first + pu / kChunks) * kBN + 64 * (w & 1);
+            mbar_arrive_expect_tx(&bars->full[st], kSlot);
+            for (int i = 0; i < 4; ++i)
+                tma_load_3d(dst + i * kVBox, &tmV, &bars->full[st], d0 + 64 * i, r0,
+                            b * p.Hkv + g);
+            ++pu;
+            return;
         }
         uint8_t *dst = ring + st * kSlot;
         mbar_arrive_expect_tx(&bars->full[st], kSlot);
@@ -253,8 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 while (pok && pu < n_loads) put();
                 if (!pok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
-                for (int w = max(0, pu - kNS); w < pu; ++w)
-                    mbar_wait(&bars->full[w % kNS], (w / kNS) & 1);
+                for (int w = max(0, pu - kNS_S); w < pu; ++w)
+                    mbar_wait(&bars->full[w % kNS_S], (w / kNS_S) & 1);
             }
             __syncwarp();
         } else if (warp == 1) {
@@ -279,8 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t dst = tmem + ((j & 1) ? TS1 : TS0);
                     for (int c = 0; c < kChunks && ok; ++c) {
-                        const int st = u % kNS;
-                        if (!(ok = mbar_wait(&bars->full[st], (u / kNS) & 1))) {
+                        const int st = u % kNS_S;
+                        if (!(ok = mbar_wait(&bars->full[st], (u / kNS_S) & 1))) {
                             set_timeout(p.status, kDiagPrefillPair, 1, 0, u);
                             break;
                         }
@@ -337,9 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bars->q_ready);
 
             const uint32_t p_full_remote = mapa_shared(smem_u32(&bars->p_full[0]), peer);
-            const uint32_t p_remote = mapa_shared(smem_u32(smem + OFF_P), peer);
-            const uint32_t f_remote = mapa_shared(smem_u32(smem + OFF_F), peer);
-            float *fst = reinterpret_cast<float *>(smem + OFF_F);
+            const uint32_t p_remote = mapa_shared(smem_u32(smem + O_OFF_P), peer);
+            const uint32_t f_remote = mapa_shared(smem_u32(smem + O_OFF_F), peer);
+            float *fst = reinterpret_cast<float *>(smem + S_OFF_F);
             float m = -CUDART_INF_F, l = 0.f;
             for (int j = 0; j < n_tiles && ok; ++j) {
                 if (!warp_wait(&bars->s_full[j & 1], (j >> 1) & 1)) {
@@ -393,14 +425,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m = m_new;
                 }
                 const float nmref = (m == -CUDART_INF_F) ? 0.f : -m;
-                // staging buffer j & 1 is free once PV(j - 2) has finished on the O-CTA
-                // (the copy out of it had landed before that PV began)
-                if (j >= 2 && !warp_wait_cluster(&bars->pfree[j & 1], ((j >> 1) + 1) & 1)) {
+                // staging buffer j & 1 is free once packet j - 2 has landed in the O-CTA
+                if (j >= 2 && !warp_wait_cluster(&bars->rack[j & 1], ((j >> 1) + 1) & 1)) {
                     set_timeout(p.status, kDiagPrefillPair, 3, 11, j);
                     ok = false;
                     break;
                 }
-                uint8_t *pbuf = smem + OFF_P + (j & 1) * kPBytes;
+                uint8_t *pbuf = smem + S_OFF_P + (j & 1) * kPBytes;
                 float2 ls[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
                 for (int c = 0; c < kBN / 32; ++c) {
@@ -429,37 +460,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();   // the bulk copy reads the packet
                 mbar_arrive(&bars->p_staged[j & 1]);
                 if (r == 0) {
+                    // receive buffer j % 3 is free once PV(j - 3) has finished
+                    const int rb = j % kNR;
                     if (!mbar_wait(&bars->p_staged[j & 1], (j >> 1) & 1)) {
                         set_timeout(p.status, kDiagPrefillPair, 3, 12, j);
                         ok = false;
+                    } else if (j >= kNR &&
+                               !mbar_wait_cluster(&bars->pfree[rb], ((j / kNR) + 1) & 1)) {
+                        set_timeout(p.status, kDiagPrefillPair, 3, 13, j);
+                        ok = false;
                     } else {
-                        const uint32_t bar = p_full_remote + (j & 1) * 8;
-                        bulk_copy_s2c(p_remote + (j & 1) * kPBytes, pbuf, kPBytes, bar);
-                        bulk_copy_s2c(f_remote + (j & 1) * kFBytes, fst + (j & 1) * kBM,
-                                      kFBytes, bar);
+                        const uint32_t bar = p_full_remote + rb * 8;
+                        bulk_copy_s2c(p_remote + rb * kPBytes, pbuf, kPBytes, bar);
+                        bulk_copy_s2c(f_remote + rb * kFBytes, fst + (j & 1) * kBM, kFBytes,
+                                      bar);
                     }
                 }
                 ok = __all_sync(0xffffffffu, ok);   // the elected lane's wait decides for its warp
             }
             if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
-            // the row sums, then the log-sum-exp
-            float *lst = reinterpret_cast<float *>(smem + OFF_L);
+            // the row sums (into the f slot of receive buffer n % 3, as reception n), then
+            // the log-sum-exp
+            float *lst = reinterpret_cast<float *>(smem + S_OFF_L);
             lst[r] = l;
             fence_proxy_async_smem();
             mbar_arrive(&bars->l_staged);
             if (valid && p.lse)
                 p.lse[((size_t)b * p.Hq + h) * p.T + t] = (m + __log2f(l)) * 0.69314718055994531f;
-            if (r == 0) {
-                if (ok && mbar_wait(&bars->l_staged, 0))
-                    bulk_copy_s2c(mapa_shared(smem_u32(lst), peer), lst, kFBytes,
-                                  mapa_shared(smem_u32(&bars->l_full), peer));
-                // the O-CTA's last arrivals on pfree land before this CTA may finish
-                for (int jj = max(0, n_tiles - 2); jj < n_tiles && ok; ++jj)
-                    if (!mbar_wait_cluster(&bars->pfree[jj & 1], (jj >> 1) & 1)) {
-                        set_timeout(p.status, kDiagPrefillPair, 3, 13, jj);
-                        set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
-                        break;
+            if (r == 0 && ok) {
+                const int rb = n_tiles % kNR;
+                if (!mbar_wait(&bars->l_staged, 0) ||
+                    (n_tiles >= kNR &&
+                     !mbar_wait_cluster(&bars->pfree[rb], ((n_tiles / kNR) + 1) & 1))) {
+                    set_timeout(p.status, kDiagPrefillPair, 3, 14, n_tiles);
+                    ok = false;
+                } else {
+                    bulk_copy_s2c(f_remote + rb * kFBytes, lst, kFBytes, p_full_remote + rb * 8);
+                }
+                // the O-CTA's last acknowledgements land before this CTA may finish
+                for (int jj = max(0, n_tiles - kNR); jj < n_tiles && ok; ++jj)
+                    if (!mbar_wait_cluster(&bars->pfree[jj % kNR], (jj / kNR) & 1)) {
+                        set_timeout(p.status, kDiagPrefillPair, 3, 15, jj);
+                        ok = false;
                     }
+                for (int jj = max(0, n_tiles - 2); jj < n_tiles && ok; ++jj)
+                    if (!mbar_wait_cluster(&bars->rack[jj & 1], (jj >> 1) & 1)) {
+                        set_timeout(p.status, kDiagPrefillPair, 3, 15, jj);
+                        ok = false;
+                    }
+                if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
             }
         }
     } else {
@@ -468,52 +517,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 while (pok && pu < n_loads) put();
                 if (!pok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
-                for (int w = max(0, pu - kNS); w < pu; ++w)
-                    mbar_wait(&bars->full[w % kNS], (w / kNS) & 1);
+                for (int w = max(0, pu - kNS_O); w < pu; ++w)
+                    mbar_wait(&bars->full[w % kNS_O], (w / kNS_O) & 1);
             }
             __syncwarp();
         } else if (warp == 1) {
             // ================= O-CTA: MMA issuer, O += P(j) V(j) =================
             if (lane == 0) {
-                const uint32_t idesc_o = idesc_bf16_f32(kBM, 128, 0, 1);
+                const uint32_t idesc_o = idesc_bf16_f32(kBM, 256, 0, 1);
                 const uint32_t rbase = smem_u32(ring);
-                const uint32_t pbase = smem_u32(smem + OFF_P);
+                const uint32_t pbase = smem_u32(smem + O_OFF_P);
                 bool ok = true;
                 int u = 0;
                 for (int j = 0; j < n_tiles && ok; ++j) {
-                    if (!(ok = mbar_wait_cluster(&bars->p_full[j & 1], (j >> 1) & 1))) {
+                    const int rb = j % kNR;
+                    if (!(ok = mbar_wait_cluster(&bars->p_full[rb], (j / kNR) & 1))) {
                         set_timeout(p.status, kDiagPrefillPair, 1, 2, j);
                         break;
                     }
-                    // arm the buffer for the packet of tile j + 2
-                    if (j + 2 < n_tiles)
-                        mbar_arrive_expect_tx(&bars->p_full[j & 1], kPBytes + kFBytes);
-                    if (!(ok = mbar_wait(&bars->o_ok[j & 1], (j >> 1) & 1))) {
+                    // arm this buffer for reception j + 3
+                    if (rx_bytes(j + kNR)) mbar_arrive_expect_tx(&bars->p_full[rb], rx_bytes(j + kNR));
+                    if (!(ok = mbar_wait(&bars->o_ok[rb], (j / kNR) & 1))) {
                         set_timeout(p.status, kDiagPrefillPair, 1, 3, j);
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t pa = pbase + (j & 1) * kPBytes;
-                    for (int c = 0; c < kChunks && ok; ++c) {
-                        const int st = u % kNS;
-                        if (!(ok = mbar_wait(&bars->full[st], (u / kNS) & 1))) {
+                    const uint32_t pa = pbase + rb * kPBytes;
+                    // chunk w = 2 dh + kh: output columns 256 dh .., keys 64 kh ..
+                    for (int w = 0; w < kChunks && ok; ++w) {
+                        const int st = u % kNS_O, dh = w >> 1, kh = w & 1;
+                        if (!(ok = mbar_wait(&bars->full[st], (u / kNS_O) & 1))) {
                             set_timeout(p.status, kDiagPrefillPair, 1, 0, u);
                             break;
                         }
                         tc_fence_after();
                         const uint32_t va = rbase + st * kSlot;
 #pragma unroll
-                        for (int kk = 0; kk < kBN / 16; ++kk) {
-                            const uint64_t ad =
-                                sdesc_sw128(pa + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-                            umma_ss(tmem + TO + 128 * c, ad, sdesc_sw128(va + kk * 2048, kBox, 1024),
-                                    idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = sdesc_sw128(pa + kh * kBox + kk * 32, 16, 1024);
+                            umma_ss(tmem + TO + 256 * dh, ad,
+                                    sdesc_sw128(va + kk * 2048, kVBox, 1024), idesc_o,
+                                    (j > 0 || kh > 0 || kk > 0) ? 1u : 0u);
                         }
                         umma_commit(&bars->empty[st]);
                         ++u;
                     }
                     if (!ok) break;
-                    umma_commit(&bars->pv_done[j & 1]);
+                    umma_commit(&bars->pv_done[rb]);
                     if (j == n_tiles - 1) umma_commit(&bars->o_final);
                 }
                 if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
@@ -526,12 +576,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 const uint32_t pfree_remote = mapa_shared(smem_u32(&bars->pfree[0]), peer);
                 for (int j = 0; j < n_tiles; ++j) {
-                    if (!mbar_wait(&bars->pv_done[j & 1], (j >> 1) & 1)) {
+                    if (!mbar_wait(&bars->pv_done[j % kNR], (j / kNR) & 1)) {
                         set_timeout(p.status, kDiagPrefillPair, 2, 14, j);
                         set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
                         break;
                     }
-                    mbar_arrive_remote(pfree_remote + (j & 1) * 8);
+                    mbar_arrive_remote(pfree_remote + (j % kNR) * 8);
+                }
+            }
+            __syncwarp();
+        } else if (warp == 3) {
+            // ======== O-CTA: tells the S-CTA that packet j has landed (staging j & 1 free) ========
+            if (lane == 0) {
+                const uint32_t rack_remote = mapa_shared(smem_u32(&bars->rack[0]), peer);
+                for (int j = 0; j < n_tiles; ++j) {
+                    if (!mbar_wait_cluster(&bars->p_full[j % kNR], (j / kNR) & 1)) {
+                        set_timeout(p.status, kDiagPrefillPair, 2, 15, j);
+                        set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
+                        break;
+                    }
+                    mbar_arrive_remote(rack_remote + (j & 1) * 8);
                 }
             }
             __syncwarp();
@@ -539,18 +603,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ================= O-CTA: lazy rescale of O rows, epilogue =================
             const int r = (warp & 3) * 32 + lane;
             const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-            const float *frcv = reinterpret_cast<const float *>(smem + OFF_F);
+            const float *frcv = reinterpret_cast<const float *>(smem + O_OFF_F);
             bool ok = true;
             for (int j = 0; j < n_tiles && ok; ++j) {
-                if (!warp_wait_cluster(&bars->p_full[j & 1], (j >> 1) & 1)) {
+                if (!warp_wait_cluster(&bars->p_full[j % kNR], (j / kNR) & 1)) {
                     set_timeout(p.status, kDiagPrefillPair, 3, 2, j);
                     ok = false;
                     break;
                 }
-                const float f = frcv[(j & 1) * kBM + r];
+                const float f = frcv[(j % kNR) * kBM + r];
                 if (__any_sync(0xffffffffu, f != 1.0f)) {
-                    // O holds the products of tiles < j: wait for the last one
-                    if (!warp_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+                    // O holds the products of tiles < j: wait for the last one (j > 0: the
+                    // factor of the first tile is always 1)
+                    if (!warp_wait(&bars->pv_done[(j - 1) % kNR], ((j - 1) / kNR) & 1)) {
                         set_timeout(p.status, kDiagPrefillPair, 3, 7, j);
                         ok = false;
                     }
@@ -568,15 +633,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_st();
                 }
                 tc_fence_before();
-                mbar_arrive(&bars->o_ok[j & 1]);
+                mbar_arrive(&bars->o_ok[j % kNR]);
             }
             if (!ok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
-            if (ok && warp_wait(&bars->o_final, 0) && warp_wait_cluster(&bars->l_full, 0)) {
+            if (ok && warp_wait(&bars->o_final, 0) &&
+                warp_wait_cluster(&bars->p_full[n_tiles % kNR], (n_tiles / kNR) & 1)) {
                 // O / l as bf16 into the ring (every PV product has completed, so no V tile
                 // is still read), as eight 128-byte-swizzled 64-column boxes; TMA stores
                 // write them out (rows past T are clipped by the tensor map)
                 tc_fence_after();
-                const float l = reinterpret_cast<const float *>(smem + OFF_L)[r];
+                const float l = frcv[(n_tiles % kNR) * kBM + r];   // the row sums
                 const float inv_l = l > 0.f ? 1.0f / l : 0.f;
 #pragma unroll 1
                 for (int c = 0; c < kD / 32; ++c) {
@@ -644,13 +710,13 @@ EncodeTiledFn encode_fn_pair() {
     return fn;
 }
 
-// dims {d, rows, slabs}, box {64, 128, 1}, 128-byte swizzle
-bool make_map_pair(CUtensorMap *map, const void *base, int rows, int slabs) {
+// dims {d, rows, slabs}, box {64, box_rows, 1}, 128-byte swizzle
+bool make_map_pair(CUtensorMap *map, const void *base, int rows, int slabs, int box_rows) {
     EncodeTiledFn fn = encode_fn_pair();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)rows, (cuuint64_t)slabs};
     const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * 2 * rows};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -664,8 +730,8 @@ int launch_prefill_pair(const void *q, const void *k_rot, const void *v, void *o
                         int B, int T, int S, int Hq, int Hkv, int window, float scale,
                         const float *table, int *status, cudaStream_t s) {
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map_pair(&mq, q, T, B * Hq) || !make_map_pair(&mk, k_rot, S, B * Hkv) ||
-        !make_map_pair(&mv, v, S, B * Hkv) || !make_map_pair(&mo, o, T, B * Hq))
+    if (!make_map_pair(&mq, q, T, B * Hq, 128) || !make_map_pair(&mk, k_rot, S, B * Hkv, 128) ||
+        !make_map_pair(&mv, v, S, B * Hkv, 64) || !make_map_pair(&mo, o, T, B * Hq, 128))
         return GQA_ERR_CUDA;
     if (ensure_smem_attr(reinterpret_cast<const void *>(prefill_pair_kernel), kSmemBytes) !=
         cudaSuccess)
