@@ -422,7 +422,7 @@ def decode_setup(w):
     st["descs"] = st["descs0"].clone()
     st["max_len"] = max(w.global_len_range[1], w.window)
     st["o"] = torch.empty_like(st["q"])
-    st["wsb"] = gqa.gqa_decode_workspace_bytes(w.nseq, w.Hq, w.d, st["max_len"])
+    st["wsb"] = gqa.gqa_decode_workspace_bytes(w.nseq, w.Hq, w.Hkv, w.d, st["max_len"])
     st["ws"] = torch.empty(st["wsb"], dtype=torch.uint8, device="cuda")
     st["retained"] = [min(c + 1, cap) if ring else c + 1
                       for c, cap, ring in zip(x.count_before, x.cap, x.is_ring)]

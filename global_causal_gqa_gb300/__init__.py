@@ -77,7 +77,7 @@ def lib() -> ctypes.CDLL:
             "gqa_prefill_workspace_bytes": ([I, I, I, I], Z),
             "gqa_attn_prefill": ([P, P, P, P, P, I, I, I, I, I, I, I, F, P, I, I, P, Z, P], I),
             "gqa_kv_append": ([P, I, P, P, I, I, P, P], I),
-            "gqa_decode_workspace_bytes": ([I, I, I, I], Z),
+            "gqa_decode_workspace_bytes": ([I, I, I, I, I], Z),
             "gqa_attn_decode": ([P, P, I, I, I, I, F, I, P, P, P, Z, P], I),
             "gqa_attn_decode_static": ([P, P, I, I, I, I, F, I, P, P, P], I),
             "gqa_prefill_gather": ([P, P, P, I, I, I, P, P, I, P, I, P], I),
@@ -201,8 +201,8 @@ def gqa_kv_append(descs, nseq: int, k_new, v_new, Hkv: int, d: int, slots_out=No
     return _check("gqa_kv_append", st, check)
 
 
-def gqa_decode_workspace_bytes(nseq: int, Hq: int, d: int, max_len: int) -> int:
-    return lib().gqa_decode_workspace_bytes(nseq, Hq, d, max_len)
+def gqa_decode_workspace_bytes(nseq: int, Hq: int, Hkv: int, d: int, max_len: int) -> int:
+    return lib().gqa_decode_workspace_bytes(nseq, Hq, Hkv, d, max_len)
 
 
 def gqa_attn_decode(q, descs, nseq: int, Hq: int, Hkv: int, d: int, scale: float,

@@ -302,11 +302,9 @@ gqa_status gqa_kv_shared_append(gqa_kv_desc *descs, int nseq, const void *q, con
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
-size_t gqa_decode_workspace_bytes(int nseq, int Hq, int d, int max_len) {
-    if (nseq <= 0 || Hq <= 0 || d <= 0 || max_len <= 0) return 0;
-    const int ns = gqa::decode_num_splits(max_len);
-    return (gqa::decode_ml_floats(nseq, Hq, ns) + static_cast<size_t>(nseq) * Hq * ns * d) *
-           sizeof(float);
+size_t gqa_decode_workspace_bytes(int nseq, int Hq, int Hkv, int d, int max_len) {
+    if (nseq <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || max_len <= 0) return 0;
+    return gqa::decode_workspace_bytes(nseq, Hq, Hkv, d, max_len);
 }
 
 gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
@@ -320,7 +318,7 @@ gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, in
     if (!aligned16(q) || !aligned16(o) || (reinterpret_cast<uintptr_t>(descs) & 7u) ||
         (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return GQA_ERR_ALIGNMENT;
-    const size_t need = gqa_decode_workspace_bytes(nseq, Hq, d, max_len);
+    const size_t need = gqa_decode_workspace_bytes(nseq, Hq, Hkv, d, max_len);
     if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GQA_ERR_ALIGNMENT;
     int *st = status_ptr();
@@ -343,7 +341,7 @@ gqa_status gqa_attn_decode_kv_shared(const void *q, const gqa_kv_desc *descs, in
         (reinterpret_cast<uintptr_t>(descs) & 7u) ||
         (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return GQA_ERR_ALIGNMENT;
-    const size_t need = gqa_decode_workspace_bytes(nseq, Hq, d, max_len);
+    const size_t need = gqa_decode_workspace_bytes(nseq, Hq, Hkv, d, max_len);
     if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GQA_ERR_ALIGNMENT;
     int *st = status_ptr();
@@ -392,7 +390,7 @@ gqa_status gqa_attn_decode_static(const void *q, const gqa_kv_desc *descs, int n
         (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return GQA_ERR_ALIGNMENT;
     // the partials of this call must fit the fixed array
-    if (gqa_decode_workspace_bytes(nseq, Hq, d, max_len) > kDecodeStaticScratchBytes)
+    if (gqa_decode_workspace_bytes(nseq, Hq, Hkv, d, max_len) > kDecodeStaticScratchBytes)
         return GQA_ERR_WORKSPACE;
     float *scratch = decode_static_scratch();
     if (!scratch) return GQA_ERR_CUDA;

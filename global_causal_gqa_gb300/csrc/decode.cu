@@ -5,8 +5,8 @@
 // §4.5 (attention equation), §2.3 (decode reads every cached K and V once per step:
 // 4 Hkv d bytes per token and layer -- the bound this kernel is written against).
 //
-// Work split: one CTA per (split of decode_chunk(max_len) keys, sequence, block of KV
-// heads); each KV head is streamed by d/128 warps (d = 128, 256, 512), each of which owns
+// Work split: one CTA per (split of `chunk` keys, sequence, block of KV heads; the split
+// rule is decode_split below); each KV head is streamed by d/128 warps (d = 128, 256, 512), each of which owns
 // 64 pairs of the split-half RoPE in two groups of 32 -- [64 p, 64 p + 64) at d <= 256;
 // [32 p, +32) and [d/4 + 32 p, +32) at d = 512, so that the pairs p-RoPE rotates are
 // spread over two warps -- with the head-dim elements j and d/2 + j of each pair j, so
@@ -174,7 +174,8 @@ template <int PARTS, bool SHARED>   // warps per KV head: d = 128 PARTS; shared 
 __global__ void __launch_bounds__(kWarps * 32, 1)
     decode_partial_kernel(const __nv_bfloat16 *__restrict__ q,
                           const gqa_kv_desc *__restrict__ descs, int Hq, int Hkv,
-                          float scale_log2, int max_len, int nsplit, float *__restrict__ ws_ml,
+                          float scale_log2, int max_len, int chunk, int nsplit,
+                          float *__restrict__ ws_ml,
                           float *__restrict__ ws_o, int *status,
                           const float *__restrict__ k_gamma) {
     constexpr int d = kD * PARTS, parts = PARTS;
@@ -221,7 +222,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                                                                    : GQA_ERR_RANGE);
         return;
     }
-    const int chunk = decode_chunk(max_len);
+    // the host passes a multiple of 64 (decode_split); the mask states that to the
+    // compiler, which then fits the kernel in 255 registers without spilling
+    chunk &= ~63;
     const int k_start = split * chunk;
     if (k_start >= sv.R || g >= Hkv) return;
     const int k_end = min(sv.R, k_start + chunk);
@@ -411,15 +414,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
                     const int sw = lane ^ (qq << 1);
-                    const float4 t0 = stg[(4 * c + qq) * 32 + sw];
-                    const float4 t1 = stg[(8 + 4 * c + qq) * 32 + sw];
                     if constexpr (SHARED) {
                         const float2 ga = gain_pair(gA, qq), gb = gain_pair(gB, qq);
-                        gain_rotate_word(bl.k0[c], bl.k0[c + 2], qq, t0, ga, gb);
-                        gain_rotate_word(bl.k1[c], bl.k1[c + 2], qq, t1, ga, gb);
+                        gain_rotate_word(bl.k0[c], bl.k0[c + 2], qq, stg[(4 * c + qq) * 32 + sw],
+                                         ga, gb);
+                        gain_rotate_word(bl.k1[c], bl.k1[c + 2], qq,
+                                         stg[(8 + 4 * c + qq) * 32 + sw], ga, gb);
                     } else {
-                        rotate_word(bl.k0[c], bl.k0[c + 2], qq, t0);
-                        rotate_word(bl.k1[c], bl.k1[c + 2], qq, t1);
+                        rotate_word(bl.k0[c], bl.k0[c + 2], qq, stg[(4 * c + qq) * 32 + sw]);
+                        rotate_word(bl.k1[c], bl.k1[c + 2], qq, stg[(8 + 4 * c + qq) * 32 + sw]);
                     }
                 }
             } else if constexpr (SHARED) {
@@ -599,7 +602,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 // One block per (query head, sequence), one thread per head-dim element.
 __global__ void __launch_bounds__(kMaxHeadDim)
     decode_combine_kernel(const gqa_kv_desc *__restrict__ descs, int Hq, int d, int max_len,
-                          int nsplit, const float *__restrict__ ws_ml,
+                          int chunk, int nsplit, const float *__restrict__ ws_ml,
                           const float *__restrict__ ws_o, __nv_bfloat16 *__restrict__ out,
                           float *__restrict__ lse) {
     const int h = blockIdx.x, seq = blockIdx.y, dd = threadIdx.x;
@@ -607,7 +610,6 @@ __global__ void __launch_bounds__(kMaxHeadDim)
     griddep_launch_dependents();
     const SeqView sv = seq_view(descs[seq], max_len);
     if (!sv.ok) return;
-    const int chunk = decode_chunk(max_len);
     const int ns = (sv.R + chunk - 1) / chunk;
     const size_t rec = ((size_t)seq * Hq + h) * nsplit;
     float M = -CUDART_INF_F;
@@ -624,14 +626,35 @@ __global__ void __launch_bounds__(kMaxHeadDim)
 
 }  // namespace
 
-int decode_num_splits(int max_len) {
-    return (max_len + decode_chunk(max_len) - 1) / decode_chunk(max_len);
+// Keys per split: the largest of 2048, 1024, ..., 64 that still gives the grid at least
+// 128 CTAs for a batch whose every sequence held max_len keys.  Long splits amortise each
+// CTA's fixed work (query load and rotation, the first table stages, the partial it
+// writes); 128 CTAs keep most of the 152 SMs streaming.  Measured on GB300 over split
+// sizes 64 .. 2048: 2048 is fastest for the 8k-64k-token batches (PLaMo-3 and Gemma-4
+// global, plain and shared K/V); 512 for 32 rings of 1024 at d = 256 (2 CTAs per
+// sequence: 128 CTAs, 0.069 ms vs 0.072 at 256 and 0.118 at 1024) and for the 64-layer
+// step's rings of 2048 (4.68 ms vs 4.98 at 256 and 7.37 at 1024).
+DecodeSplit decode_split(int nseq, int Hkv, int d, int max_len) {
+    const int heads_per_cta = kWarps / (d / kD);
+    const long rows = static_cast<long>(nseq) * ((Hkv + heads_per_cta - 1) / heads_per_cta);
+    DecodeSplit sp;
+    sp.chunk = 2048;
+    while (sp.chunk > 64 && rows * ((max_len + sp.chunk - 1) / sp.chunk) < 128) sp.chunk >>= 1;
+    sp.nsplit = (max_len + sp.chunk - 1) / sp.chunk;
+    return sp;
+}
+
+size_t decode_workspace_bytes(int nseq, int Hq, int Hkv, int d, int max_len) {
+    const int ns = decode_split(nseq, Hkv, d, max_len).nsplit;
+    return (decode_ml_floats(nseq, Hq, ns) + static_cast<size_t>(nseq) * Hq * ns * d) *
+           sizeof(float);
 }
 
 cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq, int Hkv,
                           int d, float scale, int max_len, void *o, float *lse, float *ws,
                           int *status, cudaStream_t s, const float *k_gamma) {
-    const int nsplit = decode_num_splits(max_len);
+    const DecodeSplit sp = decode_split(nseq, Hkv, d, max_len);
+    const int nsplit = sp.nsplit;
     float *ws_ml = ws;
     float *ws_o = ws + decode_ml_floats(nseq, Hq, nsplit);   // 16-byte aligned
     const int parts = d / kD;                       // warps per KV head
@@ -651,10 +674,11 @@ cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, grid, dim3(heads * parts * 32), smem, s,
                                static_cast<const __nv_bfloat16 *>(q), descs, Hq, Hkv,
-                               scale_log2, max_len, nsplit, ws_ml, ws_o, status, k_gamma);
+                               scale_log2, max_len, sp.chunk, nsplit, ws_ml, ws_o, status,
+                               k_gamma);
     if (e != cudaSuccess) return e;
     return launch_pdl(decode_combine_kernel, dim3(Hq, nseq), dim3(d), 0, s, descs, Hq, d,
-                      max_len, nsplit, static_cast<const float *>(ws_ml),
+                      max_len, sp.chunk, nsplit, static_cast<const float *>(ws_ml),
                       static_cast<const float *>(ws_o), static_cast<__nv_bfloat16 *>(o), lse);
 }
 

@@ -53,18 +53,14 @@ cudaError_t launch_kv_append(gqa_kv_desc *descs, int nseq, const void *k_new,
                              int *status, cudaStream_t s);
 
 // Decode (decode.cu)
-// Keys per split: 1024 for long caches; 256 when max_len <= 4096, so that short caches
-// (a local layer's ring of a few thousand tokens) still give enough CTAs to fill the GPU.
-// Keys per decode split: long caches get long splits (fewer partials, longer streams per
-// CTA); short ones short splits, so a batch of short rings still fills the GPU.  Measured on
-// GB300 over batches of 8k..64k-token caches: 2048 beats 1024 on every mix (0.78-0.90 vs
-// 0.76-0.87 of the copy bandwidth); 4096 helps mixed lengths but loses on uniformly long ones.
-constexpr int kDecodeChunkLong = 2048;
-constexpr int kDecodeChunkShort = 256;
-__host__ __device__ inline int decode_chunk(int max_len) {
-    return max_len > 4096 ? kDecodeChunkLong : kDecodeChunkShort;
-}
-int decode_num_splits(int max_len);
+// The split-KV grid: `chunk` keys per split (a multiple of 16), `nsplit` splits per
+// sequence, chosen on the host from the batch shape (decode.cu documents the rule).  The
+// workspace holds nseq Hq nsplit partials, so its size and the launch use the same rule.
+struct DecodeSplit {
+    int chunk;
+    int nsplit;
+};
+DecodeSplit decode_split(int nseq, int Hkv, int d, int max_len);
 // Decode workspace layout: nseq Hq nsplit (m, l) float pairs, padded to a multiple of 4
 // floats so that the O partials after them start on a 16-byte boundary (the partial
 // kernel writes them with 16-byte stores), then nseq Hq nsplit rows of d floats.
@@ -82,6 +78,8 @@ cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int
                           int d, float scale, int max_len, void *o, float *lse,
                           float *ws, int *status, cudaStream_t s,
                           const float *k_gamma = nullptr);
+// Bytes of decode workspace for this batch shape (the same rule as launch_decode).
+size_t decode_workspace_bytes(int nseq, int Hq, int Hkv, int d, int max_len);
 
 // d = 128 prefill: picks the persistent kernel (prefill.cu) or the one-CTA-per-item
 // kernel (prefill_stream.cu) by the mean item length; returns a gqa_status

@@ -15,7 +15,7 @@ RoPE tables.
 from __future__ import annotations
 
 from dataclasses import dataclass
-from typing import List, Optional, Sequence
+from typing import List, Sequence
 
 import numpy as np
 
@@ -58,7 +58,10 @@ class LayerStack:
         dev = layers[0].q.device
         self.descs0 = torch.stack(rows).to(dev)   # [layers, nseq * sizeof(gqa_kv_desc)]
         self.descs = self.descs0.clone()
-        self.wsb = gqa_decode_workspace_bytes(self.nseq, Hq, d, max_len)
+        # a ring layer holds at most its capacity; a linear one at most max_len tokens
+        self.max_lens = [L.k_cache.shape[2] if L.is_ring else max_len for L in layers]
+        self.wsb = max(gqa_decode_workspace_bytes(self.nseq, Hq, Hkv, d, n)
+                       for n in set(self.max_lens))
         self.ws = torch.empty(self.wsb, dtype=torch.uint8, device=dev)
         self.graph = None
 
@@ -74,7 +77,7 @@ class LayerStack:
             gqa_kv_append(self.descs[l], self.nseq, L.k_new, L.v_new, self.Hkv, self.d, None,
                           stream)
             gqa_attn_decode(L.q, self.descs[l], self.nseq, self.Hq, self.Hkv, self.d,
-                            self.scale, self.max_len, L.o, None, self.ws, self.wsb, stream)
+                            self.scale, self.max_lens[l], L.o, None, self.ws, self.wsb, stream)
 
     def capture(self):
         """Captures `step` (with the count restore) in a CUDA graph on a side stream."""

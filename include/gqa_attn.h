@@ -256,12 +256,14 @@ gqa_status gqa_kv_shared_append(gqa_kv_desc *descs, int nseq, const void *q, con
  * with the sequence's table.  o: [nseq, Hq, d] bf16; lse: [nseq, Hq] float or NULL.
  * max_len: an upper bound on R over the batch (sizes the split-KV grid); a sequence with
  * R > max_len or rope_len < R is skipped and flagged in the status word.
- * workspace: device scratch of gqa_decode_workspace_bytes(nseq, Hq, d, max_len) bytes:
+ * workspace: device scratch of gqa_decode_workspace_bytes(nseq, Hq, Hkv, d, max_len) bytes:
  * the split partials, nseq Hq nsplit (m, l) float pairs padded to a multiple of 4 floats,
- * then nseq Hq nsplit rows of d floats, nsplit = ceil(max_len / chunk) with chunk = 2048
- * keys when max_len > 4096 and 256 otherwise.  scale: finite and > 0.
+ * then nseq Hq nsplit rows of d floats.  The number of splits per sequence, nsplit, and
+ * the keys per split are chosen from (nseq, Hkv, d, max_len) so that the grid fills the
+ * GPU; the workspace size follows the same rule, so it must be queried with the shape of
+ * the call.  scale: finite and > 0.
  * d in {128, 256, 512} (Gemma-4 local / global heads), Hq/Hkv <= 8. */
-size_t gqa_decode_workspace_bytes(int nseq, int Hq, int d, int max_len);
+size_t gqa_decode_workspace_bytes(int nseq, int Hq, int Hkv, int d, int max_len);
 gqa_status gqa_attn_decode(const void *q, const gqa_kv_desc *descs, int nseq, int Hq,
                            int Hkv, int d, float scale, int max_len, void *o, float *lse,
                            void *workspace, size_t workspace_bytes, gqa_stream_t stream);
@@ -279,7 +281,7 @@ gqa_status gqa_attn_decode_kv_shared(const void *q, const gqa_kv_desc *descs, in
  * because the device synchronisation of cudaMalloc/cudaFree is unacceptable per step.
  * The split-KV partials go to a fixed 16 MiB device array inside the library, which every
  * GPU that loads the library holds until the process exits.  A call whose partials need
- * more than that, i.e. gqa_decode_workspace_bytes(nseq, Hq, d, max_len) > 16 MiB, returns
+ * more than that, i.e. gqa_decode_workspace_bytes(nseq, Hq, Hkv, d, max_len) > 16 MiB, returns
  * GQA_ERR_WORKSPACE without launching.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  * with that device current; make that first call before any stream capture.

@@ -41,10 +41,16 @@ def test_yarn_amplitude_and_sizes():
     assert abs(gqa.gqa_yarn_amplitude(256.0) - (1 + 0.1 * math.log(256))) < 1e-15
     assert gqa.gqa_rope_table_bytes(128, 1000) == 1000 * 64 * 2 * 4
     assert gqa.gqa_prefill_workspace_bytes(2, 8, 8192, 128) == 2 * 8 * 8192 * 128 * 2
-    assert gqa.gqa_decode_workspace_bytes(32, 64, 128, 65536) == 32 * 64 * 32 * 130 * 4  # 2048-key splits
-    # short caches split every 256 keys
-    assert gqa.gqa_decode_workspace_bytes(32, 16, 256, 1024) == 32 * 16 * 4 * 258 * 4
-    assert gqa.gqa_decode_workspace_bytes(2, 8, 512, 4097) == 2 * 8 * 3 * 514 * 4
+    # decode: a whole number of splits per (sequence, query head), each a partial of d + 2
+    # floats, at least one split and no more than one per 16 keys
+    for args in [(32, 64, 8, 128, 65536), (32, 16, 8, 256, 1024), (2, 8, 1, 512, 4097),
+                 (1, 1, 1, 128, 1)]:
+        nseq, Hq, Hkv, d, max_len = args
+        total = gqa.gqa_decode_workspace_bytes(*args)
+        ns = (total // 4) // (nseq * Hq * (d + 2))
+        assert 1 <= ns <= -(-max_len // 16), args
+        assert total == 4 * (-(-2 * nseq * Hq * ns // 4) * 4 + nseq * Hq * ns * d), args
+    assert gqa.gqa_decode_workspace_bytes(2, 8, 0, 128, 64) == 0
     assert gqa.gqa_rope_table_bytes(0, 10) == 0
 
 
@@ -59,9 +65,9 @@ def test_decode_workspace_layout_keeps_partials_aligned():
         for Hq in (1, 2, 3, 5, 7, 64):
             for d in (128, 256, 512):
                 for max_len in (1, 256, 257, 768, 1280, 4096, 4097, 6145, 65536):
-                    chunk = 2048 if max_len > 4096 else 256
-                    ns = -(-max_len // chunk)
-                    total = gqa.gqa_decode_workspace_bytes(nseq, Hq, d, max_len)
+                    Hkv = 1
+                    total = gqa.gqa_decode_workspace_bytes(nseq, Hq, Hkv, d, max_len)
+                    ns = (total // 4) // (nseq * Hq * (d + 2))   # splits per sequence
                     head = total - nseq * Hq * ns * d * 4
                     pairs = 2 * nseq * Hq * ns * 4
                     assert head % 16 == 0, (nseq, Hq, d, max_len)
@@ -74,7 +80,7 @@ def test_non_positive_scale_rejected_on_host():
     L = gqa.lib()
     S = gqa.STATUS_NAMES
     fake = 0x10000
-    wsb = gqa.gqa_decode_workspace_bytes(1, 2, 128, 64)
+    wsb = gqa.gqa_decode_workspace_bytes(1, 2, 1, 128, 64)
     for bad in (0.0, -0.125, float("-inf"), float("nan")):
         assert S[L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 2, 1, 128, 0, bad,
                                     fake, 8, 1, None, 0, None)] == "GQA_ERR_INVALID_ARG"
@@ -172,7 +178,7 @@ def test_kv_shared_arguments_rejected_on_host():
     assert f(L.gqa_kv_shared_append(fake, 1, fake, fake, 2, 1, 128, fake, -1.0, fake, None,
                                     None)) == "GQA_ERR_INVALID_ARG"
     # decode: no key gain, head dim 64, group of 16, too little workspace, misaligned gain
-    wsb = gqa.gqa_decode_workspace_bytes(1, 2, 128, 64)
+    wsb = gqa.gqa_decode_workspace_bytes(1, 2, 1, 128, 64)
     assert f(L.gqa_attn_decode_kv_shared(fake, fake, 1, 2, 1, 128, 1.0, None, 64, fake, None,
                                          fake, wsb, None)) == "GQA_ERR_INVALID_ARG"
     assert f(L.gqa_attn_decode_kv_shared(fake, fake, 1, 2, 1, 64, 1.0, fake, 64, fake, None,

@@ -56,7 +56,7 @@ def run_step(st: DecodeSetup, Hq: int, Hkv: int, scale: float, max_len: int):
     gqa.gqa_kv_append(st.descs, nseq, st.k_new, st.v_new, Hkv, st.d, slots)
     o = torch.empty_like(st.q)
     lse = torch.empty(nseq, Hq, dtype=torch.float32, device="cuda")
-    wsb = gqa.gqa_decode_workspace_bytes(nseq, Hq, st.d, max_len)
+    wsb = gqa.gqa_decode_workspace_bytes(nseq, Hq, Hkv, st.d, max_len)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     gqa.gqa_attn_decode(st.q, st.descs, nseq, Hq, Hkv, st.d, scale, max_len, o, lse, ws, wsb)
     status = gqa.gqa_get_device_status()
@@ -213,7 +213,7 @@ def test_prope_unrotated_parts_match_rotation():
     descs2 = torch.from_numpy(a.view(np.uint8).copy()).cuda()
     o2 = torch.empty_like(st.q)
     lse2 = torch.empty_like(lse1)
-    wsb = gqa.gqa_decode_workspace_bytes(3, Hq, d, 4096)
+    wsb = gqa.gqa_decode_workspace_bytes(3, Hq, Hkv, d, 4096)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     gqa.gqa_attn_decode(st.q, descs2, 3, Hq, Hkv, d, scale, 4096, o2, lse2, ws, wsb)
     assert gqa.gqa_get_device_status() == 0
@@ -221,11 +221,12 @@ def test_prope_unrotated_parts_match_rotation():
     assert torch.equal(lse1, lse2)
 
 
-def test_long_split_boundaries():
-    """max_len > 4096 (2048-key splits): caches ending just before, at and after split
-    boundaries, a split that holds a single key, and rings that wrap."""
+@pytest.mark.parametrize("Hq,Hkv", [(16, 2), (32, 32)])
+def test_long_split_boundaries(Hq, Hkv):
+    """max_len 8192: caches ending just before, at and after split boundaries, a split
+    that holds a single key, and rings that wrap.  With 2 KV heads the batch gets 512-key
+    splits; with 32 (four CTAs of 8 heads per sequence) the longest, 2048-key splits."""
     gu.require_gpu()
-    Hq, Hkv = 16, 2
     lengths = [2047, 2048, 2049, 4095, 4096, 4097, 6143]
     rings = [(2048, 2047), (2048, 5000)]
     x = _random_batch(lengths, rings, Hq, Hkv, seed=77)
@@ -235,27 +236,27 @@ def test_long_split_boundaries():
     ro, rl, rslots, rcounts = oracle_step(x, 128, scale)
     assert np.array_equal(slots.cpu().numpy().astype(np.int64), rslots)
     assert np.array_equal(st.counts(), rcounts)
-    gu.compare(o, ro, what="decode, 2048-key splits")
-    gu.compare(lse, rl, what="decode lse, 2048-key splits")
+    gu.compare(o, ro, what=f"decode, long splits, Hkv={Hkv}")
+    gu.compare(lse, rl, what=f"decode lse, long splits, Hkv={Hkv}")
 
 
 @pytest.mark.parametrize("nseq_lin,Hq,Hkv,d,max_len",
-                         [(1, 1, 1, 128, 256), (3, 3, 1, 128, 768), (1, 5, 1, 256, 256),
-                          (3, 7, 1, 128, 1280), (1, 3, 1, 512, 768), (3, 1, 1, 128, 6144)])
+                         [(1, 1, 1, 128, 64), (3, 3, 1, 128, 320), (1, 5, 1, 256, 192),
+                          (3, 7, 1, 128, 448), (1, 3, 1, 512, 320), (3, 1, 1, 128, 6208)])
 def test_odd_partial_counts(nseq_lin, Hq, Hkv, d, max_len):
     """nseq * Hq * nsplit odd: the (m, l) pairs of the workspace fill an odd number of
     8-byte slots, and the O partials after them must still start on a 16-byte boundary
-    (they are written with 16-byte stores).  One ring per batch keeps nseq odd when a
-    linear count is even."""
+    (they are written with 16-byte stores).  The split count is read back from the
+    workspace size (whole partials of d + 2 floats per sequence, head and split)."""
     gu.require_gpu()
     lengths = [max_len - 1 - 97 * i for i in range(nseq_lin - 1)] + [min(40, max_len - 1)]
-    rings = [] if nseq_lin % 2 else [(64, 150)]
-    x = _random_batch(lengths, rings, Hq, Hkv, d, seed=1000 + Hq * 10 + nseq_lin)
+    x = _random_batch(lengths, [], Hq, Hkv, d, seed=1000 + Hq * 10 + nseq_lin)
     if d == 512:
-        x = replace(x, rope=[PROPE if not r else LOCAL for r in x.is_ring])
-    nseq = len(lengths) + len(rings)
-    chunk = 2048 if max_len > 4096 else 256
-    assert (nseq * Hq * -(-max_len // chunk)) % 2 == 1
+        x = replace(x, rope=[PROPE] * len(lengths))
+    nseq = len(lengths)
+    wsb = gqa.gqa_decode_workspace_bytes(nseq, Hq, Hkv, d, max_len)
+    nsplit = (wsb // 4) // (nseq * Hq * (d + 2))
+    assert (nseq * Hq * nsplit) % 2 == 1, nsplit
     st = DecodeSetup(x, d)
     scale = 1 / math.sqrt(d)
     o, lse, slots = run_step(st, Hq, Hkv, scale, max_len=max_len)

@@ -103,7 +103,7 @@ def _shared_step(st, x, Hq, Hkv, d, gq, gk, max_len, scale=1.0):
                              q_out, slots)
     o = torch.empty_like(st.q)
     lse = torch.empty(nseq, Hq, dtype=torch.float32, device="cuda")
-    wsb = gqa.gqa_decode_workspace_bytes(nseq, Hq, d, max_len)
+    wsb = gqa.gqa_decode_workspace_bytes(nseq, Hq, Hkv, d, max_len)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     gqa.gqa_attn_decode_kv_shared(q_out, st.descs, nseq, Hq, Hkv, d, scale, _dev_gain(gk),
                                   max_len, o, lse, ws, wsb)
@@ -156,7 +156,7 @@ def test_decode_kv_shared(Hq, Hkv, d):
 
 
 def test_decode_kv_shared_long_splits():
-    """max_len > 4096 (2048-key splits) with split-boundary lengths, d = 512."""
+    """max_len 8192 with lengths at split boundaries, d = 512."""
     gu.require_gpu()
     Hq, Hkv, d = 16, 2, 512
     x = _random_batch([2047, 2048, 2049, 4100], [(1024, 3000)], Hq, Hkv, d, seed=2100)
@@ -168,7 +168,7 @@ def test_decode_kv_shared_long_splits():
     e2e = _oracle_shared(x, d, gq, gk)
     assert np.array_equal(slots.cpu().numpy().astype(np.int64), e2e[2])
     assert np.array_equal(st.counts(), e2e[3])
-    _check_decode(o, lse, e2e, "kv-shared decode, 2048-key splits")
+    _check_decode(o, lse, e2e, "kv-shared decode, long caches")
 
 
 def test_decode_kv_shared_equals_separate_caches():
@@ -195,7 +195,7 @@ def test_decode_kv_shared_equals_separate_caches():
                            [st.tables[r][1] for r in x.rope])
     descs_sh = torch.from_numpy(a2.view(np.uint8).copy()).cuda()
     nseq, max_len = x.q.shape[0], 4096
-    wsb = gqa.gqa_decode_workspace_bytes(nseq, Hq, d, max_len)
+    wsb = gqa.gqa_decode_workspace_bytes(nseq, Hq, Hkv, d, max_len)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     o1, o2 = torch.empty_like(st.q), torch.empty_like(st.q)
     gqa.gqa_attn_decode(st.q, descs_sep, nseq, Hq, Hkv, d, 0.05, max_len, o1, None, ws, wsb)

@@ -111,7 +111,7 @@ def test_decode_norm_append_then_attend(v_norm):
                            EPS, v_norm, q_out, slots)
     o = torch.empty_like(st.q)
     max_len = 1024
-    wsb = gqa.gqa_decode_workspace_bytes(nseq, Hq, d, max_len)
+    wsb = gqa.gqa_decode_workspace_bytes(nseq, Hq, Hkv, d, max_len)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     scale = 1 / math.sqrt(d)
     gqa.gqa_attn_decode(q_out, st.descs, nseq, Hq, Hkv, d, scale, max_len, o, None, ws, wsb)

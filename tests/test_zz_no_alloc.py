@@ -66,7 +66,7 @@ class _Dev:
 def _workspace_decode(dev, Hq, Hkv, max_len, scale):
     o = torch.empty_like(dev.q)
     lse = torch.empty(dev.n, Hq, dtype=torch.float32, device="cuda")
-    wsb = gqa.gqa_decode_workspace_bytes(dev.n, Hq, 128, max_len)
+    wsb = gqa.gqa_decode_workspace_bytes(dev.n, Hq, Hkv, 128, max_len)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     gqa.gqa_attn_decode(dev.q, dev.descs, dev.n, Hq, Hkv, 128, scale, max_len, o, lse, ws, wsb)
     assert gqa.gqa_get_device_status() == 0
@@ -84,16 +84,20 @@ def _static_decode(dev, Hq, Hkv, max_len, scale):
 def test_static_matches_workspace_decode_twice():
     gu.require_gpu()
     scale = 1 / math.sqrt(128)
-    # call A: 8 sequences, 64/8 heads, max_len 8192 (2048-key splits, 4 per sequence)
+    # call A: 8 sequences, 64/8 heads, max_len 8192
     a_shape = dict(Hq=64, Hkv=8, max_len=8192)
     dev_a = _Dev(_batch(1, [3, 1000, 2049, 4000, 8000], [(2048, 2047), (2048, 9000), (64, 70)],
                         a_shape["Hq"], a_shape["Hkv"]))
-    # call B: 3 sequences, 3/1 heads, max_len 768 (256-key splits, 3 per sequence): every
-    # record sits at another offset than in call A, and nseq*Hq*nsplit = 27 is odd
-    b_shape = dict(Hq=3, Hkv=1, max_len=768)
+    # call B: 3 sequences, 3/1 heads, max_len 704: another split layout, so every record
+    # sits at another offset than in call A, and nseq * Hq * nsplit is odd
+    b_shape = dict(Hq=3, Hkv=1, max_len=704)
     dev_b = _Dev(_batch(2, [700, 5], [(256, 300)], b_shape["Hq"], b_shape["Hkv"]))
+    splits = []
     for dev, shp in ((dev_a, a_shape), (dev_b, b_shape)):
-        assert gqa.gqa_decode_workspace_bytes(dev.n, shp["Hq"], 128, shp["max_len"]) <= STATIC_BYTES
+        wsb = gqa.gqa_decode_workspace_bytes(dev.n, shp["Hq"], shp["Hkv"], 128, shp["max_len"])
+        assert wsb <= STATIC_BYTES
+        splits.append((wsb // 4) // (dev.n * shp["Hq"] * 130))
+    assert splits[0] != splits[1] and (dev_b.n * b_shape["Hq"] * splits[1]) % 2 == 1
     ref_a = _workspace_decode(dev_a, scale=scale, **a_shape)
     ref_b = _workspace_decode(dev_b, scale=scale, **b_shape)
     # two calls in a row; the second must read none of the first's partials
@@ -117,7 +121,7 @@ def test_static_rejects_oversize_without_launch():
     Hq, Hkv = 64, 8
     dev = _Dev(_batch(3, [3, 1000], [(64, 70)], Hq, Hkv))
     max_len = 1 << 20                      # partials far beyond the 16 MiB array
-    assert gqa.gqa_decode_workspace_bytes(dev.n, Hq, 128, max_len) > STATIC_BYTES
+    assert gqa.gqa_decode_workspace_bytes(dev.n, Hq, Hkv, 128, max_len) > STATIC_BYTES
     o = torch.zeros_like(dev.q)
     st = gqa.gqa_attn_decode_static(dev.q, dev.descs, dev.n, Hq, Hkv, 128, 0.1, max_len, o,
                                     None, check=False)
