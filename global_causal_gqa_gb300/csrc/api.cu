@@ -159,10 +159,11 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
         if (!aligned16(workspace)) return GQA_ERR_ALIGNMENT;
     }
     // the grid: one CTA per (b, KV head, head pair, 128-row block) for d = 128, per
-    // (b, head, 128-row block, output slice) for d = 256 / 512
+    // (b, head, 128-row block) for d = 256, four per (b, KV head, head pair, 128-row block)
+    // for d = 512
     const long mblocks = (T + 127) / 128;
-    const long blocks = d == 128 ? static_cast<long>(B) * Hkv * ((Hq / Hkv + 1) / 2) * mblocks
-                                 : static_cast<long>(B) * Hq * mblocks * (d == 512 ? 2 : 1);
+    const long hpairs = static_cast<long>(B) * Hkv * ((Hq / Hkv + 1) / 2) * mblocks;
+    const long blocks = d == 128 ? hpairs : d == 512 ? 4 * hpairs : static_cast<long>(B) * Hq * mblocks;
     if (blocks > 0x7fffffffL) return GQA_ERR_UNSUPPORTED;
     int *st = status_ptr();
     if (!st) return GQA_ERR_CUDA;

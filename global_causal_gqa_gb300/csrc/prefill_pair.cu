@@ -1,5 +1,5 @@
-// prefill_pair.cu -- causal / sliding-window GQA prefill for d = 512 heads on a pair of
-// CTAs (a thread-block cluster of two), each score tile computed once.
+// prefill_pair.cu -- causal / sliding-window GQA prefill for d = 512 heads on pairs of CTAs
+// (two pairs per thread-block cluster), each score tile computed once.
 //
 // Same computation as prefill_wide.cu ("PLaMo 3アーキテクチャ徹底解析" §4.5, §5.1; the
 // Gemma-4 global layer of the qiita.com Gemma-4-26B-A4B explainer, with the p-RoPE of
@@ -27,8 +27,17 @@
 // core's completion: receive buffer j % 3 is free for packet j + 3).  Three receive
 // buffers keep the loop packet -> PV -> acknowledgement -> next packet off the tensor
 // pipe's critical path.
-// Every wait is bounded; both CTAs meet at a cluster barrier before either exits, so no
-// copy or remote arrival targets the shared memory of a CTA that has finished.
+// A cluster holds two such pairs, for two query heads of one KV group (ranks 0, 1: their
+// S-CTAs; 2, 3: their O-CTAs).  The two S-CTAs read the same K tiles and the two O-CTAs the
+// same V tiles, so each chunk is loaded once and multicast to both: each CTA issues every
+// other chunk of its ring, arms its own "full" barrier for every chunk, and a slot is
+// reloaded once both CTAs' MMAs have released it (their completions are multicast onto
+// both "empty" barriers).  This halves the L2-to-SM traffic of a key tile; a CTA alone
+// could not keep its tensor pipe fed from 5 slots in flight.  With an odd group size the
+// last pair computes its group's last head a second time and stores nothing.
+// Every wait is bounded; the four CTAs meet at a cluster barrier before any exits, so no
+// copy, multicast load or remote arrival targets the shared memory of a CTA that has
+// finished.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -77,7 +86,7 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t TQ = 0, TS0 = 256, TS1 = 384, TO = 0;
 
 struct PBars {
-    uint64_t full[kNS_S], empty[kNS_S];   // ring (both; the O-CTA uses kNS_O)
+    uint64_t full[kNS_S], empty[kNS_S];   // ring (both; the O-CTA uses kNS_O); empty: 2
     uint64_t q_rot;                   // S: Q rotated in shared memory (256 arrivals)
     uint64_t q_ready;                 // S: Q in TMEM (128)
     uint64_t s_full[2], s_free[2];    // S: score buffer written / read out (128)
@@ -100,7 +109,7 @@ struct PairParams {
     const float2 *table;
     int *status;
     int T, S, Hq, Hkv, G, window;
-    int n_mblocks;
+    int n_mblocks, n_hpairs;   // query blocks; head pairs per KV group, ceil(G / 2)
     float scale_log2;
 };
 
@@ -122,15 +131,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     PBars *bars = reinterpret_cast<PBars *>(smem + OFF_BAR);
     uint8_t *ring = smem;   // the ring starts the layout in both CTAs
     const uint32_t rank = cluster_ctarank();
-    const bool is_s = rank == 0;
+    const bool is_s = rank < 2;
+    const int sub = static_cast<int>(rank & 1);          // which head of the cluster's pair
+    const uint16_t role_mask = is_s ? 0x3 : 0xC;           // the CTAs sharing this ring
+    const uint32_t sibling = rank ^ 1u;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int idx = blockIdx.x >> 1;
-    const int h = idx % p.Hq;
-    idx /= p.Hq;
+    int idx = blockIdx.x >> 2;
+    const int hpi = idx % (p.Hkv * p.n_hpairs);
+    idx /= p.Hkv * p.n_hpairs;
     const int mb = p.n_mblocks - 1 - (idx % p.n_mblocks);   // longest rows first
     const int b = idx / p.n_mblocks;
-    const int g = h / p.G;
+    const int g = hpi / p.n_hpairs;
+    const int hg = 2 * (hpi % p.n_hpairs) + sub;           // head within the group
+    const bool dup = hg >= p.G;                              // odd group: a repeat, not stored
+    const int h = g * p.G + (dup ? p.G - 1 : hg);
     const int q_lo = p.S - p.T + mb * kBM;
     const int q_hi = min(q_lo + kBM - 1, p.S - 1);
     const int kt_first = p.window > 0 ? max(0, q_lo - p.window + 1) / kBN : 0;
@@ -148,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNS_S; ++i) {
             mbar_init(&bars->full[i], 1);
-            mbar_init(&bars->empty[i], 1);
+            mbar_init(&bars->empty[i], 2);   // this CTA's MMA and its sibling's
         }
         mbar_init(&bars->q_rot, kThreads);
         mbar_init(&bars->q_ready, 128);
@@ -183,14 +198,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();   // both CTAs' barriers exist before any remote copy or arrival
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const uint32_t peer = is_s ? 1u : 0u;
+    const uint32_t peer = rank ^ 2u;   // the other role of this head's pair
 
     // ---- ring producer state (warp 0, lane 0) ----
     int pu = 0;
     bool pok = true;
     auto put = [&]() {
         const int st = pu % kNS;
-        if (pu >= kNS && !(pok = mbar_wait(&bars->empty[st], ((pu / kNS) - 1) & 1))) {
+        if (pu >= kNS && !(pok = mbar_wait_cluster(&bars->empty[st], ((pu / kNS) - 1) & 1))) {
             set_timeout(p.status, kDiagPrefillPair, 0, 1, pu);
             return;
         }
@@ -202,20 +217,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             c1 = mb * kBM;
             c2 = b * p.Hq + h;
         } else if (is_s) {
+            // K chunk v of the shared stream: armed here, loaded by one of the two S-CTAs
             const int v = pu - n_q;
-            map = &tmK;
-            c0 = 128 * (v % kChunks);
-            c1 = (kt_first + v / kChunks) * kBN;
-            c2 = b * p.Hkv + g;
+            uint8_t *dst = ring + st * kSlot;
+            mbar_arrive_expect_tx(&bars->full[st], kSlot);
+            if ((v & 1) == sub) {
+                const int k0 = 128 * (v % kChunks), r0 = (kt_first + v / kChunks) * kBN;
+                tma_load_3d_mc(dst, &tmK, &bars->full[st], k0, r0, b * p.Hkv + g, role_mask);
+                tma_load_3d_mc(dst + kBox, &tmK, &bars->full[st], k0 + 64, r0, b * p.Hkv + g,
+                               role_mask);
+            }
+            ++pu;
+            return;
         } else {
-            // four 64 x 64 boxes: dims 256 dh + 64 i, keys 64 kh .. 64 kh + 63
+            // V chunk pu, four 64 x 64 boxes: dims 256 dh + 64 i, keys 64 kh .. 64 kh + 63;
+            // armed here, loaded by one of the two O-CTAs
             const int w = pu % kChunks;
             uint8_t *dst = ring + st * kSlot;
             const int d0 = 256 * (w >> 1), r0 = (kt_first + pu / kChunks) * kBN + 64 * (w & 1);
             mbar_arrive_expect_tx(&bars->full[st], kSlot);
-            for (int i = 0; i < 4; ++i)
-                tma_load_3d(dst + i * kVBox, &tmV, &bars->full[st], d0 + 64 * i, r0,
-                            b * p.Hkv + g);
+            if ((pu & 1) == sub)
+                for (int i = 0; i < 4; ++i)
+                    tma_load_3d_mc(dst + i * kVBox, &tmV, &bars->full[st], d0 + 64 * i, r0,
+                                   b * p.Hkv + g, role_mask);
             ++pu;
             return;
         }
@@ -297,8 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = mbar_wait(&bars->q_ready, 0);
                 if (!ok) set_timeout(p.status, kDiagPrefillPair, 1, 4, 0);
                 tc_fence_after();
-                // the Q slots are free for K once Q has been copied into TMEM
-                for (int i = 0; i < 4; ++i) mbar_arrive(&bars->empty[i]);
+                // the Q slots are free for K once Q has been copied into TMEM (here and,
+                // for the sibling's loads into them, there)
+                const uint32_t empty_sib = mapa_shared(smem_u32(&bars->empty[0]), sibling);
+                for (int i = 0; i < 4; ++i) {
+                    mbar_arrive(&bars->empty[i]);
+                    mbar_arrive_remote(empty_sib + 8 * i);
+                }
                 int u = n_q;
                 for (int j = 0; j < n_tiles && ok; ++j) {
                     if (j >= 2) {
@@ -312,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t dst = tmem + ((j & 1) ? TS1 : TS0);
                     for (int c = 0; c < kChunks && ok; ++c) {
                         const int st = u % kNS_S;
-                        if (!(ok = mbar_wait(&bars->full[st], (u / kNS_S) & 1))) {
+                        if (!(ok = mbar_wait_cluster(&bars->full[st], (u / kNS_S) & 1))) {
                             set_timeout(p.status, kDiagPrefillPair, 1, 0, u);
                             break;
                         }
@@ -326,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             umma_ts(dst, tmem + TQ + 8 * dk, bd, idesc_s,
                                     (c > 0 || kk > 0) ? 1u : 0u);
                         }
-                        umma_commit(&bars->empty[st]);
+                        umma_commit_mc(&bars->empty[st], role_mask);
                         ++u;
                     }
                     if (ok) umma_commit(&bars->s_full[j & 1]);
@@ -485,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             lst[r] = l;
             fence_proxy_async_smem();
             mbar_arrive(&bars->l_staged);
-            if (valid && p.lse)
+            if (valid && p.lse && !dup)
                 p.lse[((size_t)b * p.Hq + h) * p.T + t] = (m + __log2f(l)) * 0.69314718055994531f;
             if (r == 0 && ok) {
                 const int rb = n_tiles % kNR;
@@ -546,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // chunk w = 2 dh + kh: output columns 256 dh .., keys 64 kh ..
                     for (int w = 0; w < kChunks && ok; ++w) {
                         const int st = u % kNS_O, dh = w >> 1, kh = w & 1;
-                        if (!(ok = mbar_wait(&bars->full[st], (u / kNS_O) & 1))) {
+                        if (!(ok = mbar_wait_cluster(&bars->full[st], (u / kNS_O) & 1))) {
                             set_timeout(p.status, kDiagPrefillPair, 1, 0, u);
                             break;
                         }
@@ -559,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     sdesc_sw128(va + kk * 2048, kVBox, 1024), idesc_o,
                                     (j > 0 || kh > 0 || kk > 0) ? 1u : 0u);
                         }
-                        umma_commit(&bars->empty[st]);
+                        umma_commit_mc(&bars->empty[st], role_mask);
                         ++u;
                     }
                     if (!ok) break;
@@ -666,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&bars->staged);
-                if (r == 0) {
+                if (r == 0 && !dup) {
                     if (!mbar_wait(&bars->staged, 0)) {
                         set_timeout(p.status, kDiagPrefillPair, 3, 10, n_tiles);
                     } else {
@@ -747,16 +776,17 @@ int launch_prefill_pair(const void *q, const void *k_rot, const void *v, void *o
     p.G = Hq / Hkv;
     p.window = window;
     p.n_mblocks = (T + kBM - 1) / kBM;
+    p.n_hpairs = (p.G + 1) / 2;
     p.scale_log2 = scale * 1.4426950408889634f;
-    const long pairs = (long)B * Hq * p.n_mblocks;
+    const long clusters = (long)B * Hkv * p.n_hpairs * p.n_mblocks;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.gridDim = dim3(static_cast<unsigned>(4 * clusters));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = 4;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;

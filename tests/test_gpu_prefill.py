@@ -132,6 +132,10 @@ WIDE_CASES = [
     _layer(1, 300, 300, 4, 2, 0, PROPE, d=512, seed=73),
     _layer(1, 65, 500, 8, 2, 100, PROPE, d=512, seed=74),
     _layer(1, 1, 1, 2, 1, 0, d=512, seed=75),
+    # odd groups at d = 512: the cluster's second head pair repeats the group's last head
+    _layer(1, 260, 260, 3, 1, 0, PROPE, d=512, seed=76),
+    _layer(1, 200, 330, 6, 2, 70, PROPE, d=512, seed=77),
+    _layer(2, 129, 129, 2, 2, 0, d=512, seed=78),
 ]
 
 
