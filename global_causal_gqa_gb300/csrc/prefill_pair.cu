@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool pok = true;
     auto put = [&]() {
         const int st = pu % kNS;
-        if (pu >= kNS && !(pok = mbar_wait_cluster(&bars->empty[st], ((pu / kNS) - 1) & 1))) {
+        if (pu >= kNS && !(pok = mbar_wait(&bars->empty[st], ((pu / kNS) - 1) & 1))) {
             set_timeout(p.status, kDiagPrefillPair, 0, 1, pu);
             return;
         }
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t dst = tmem + ((j & 1) ? TS1 : TS0);
                     for (int c = 0; c < kChunks && ok; ++c) {
                         const int st = u % kNS_S;
-                        if (!(ok = mbar_wait_cluster(&bars->full[st], (u / kNS_S) & 1))) {
+                        if (!(ok = mbar_wait(&bars->full[st], (u / kNS_S) & 1))) {
                             set_timeout(p.status, kDiagPrefillPair, 1, 0, u);
                             break;
                         }
@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // chunk w = 2 dh + kh: output columns 256 dh .., keys 64 kh ..
                     for (int w = 0; w < kChunks && ok; ++w) {
                         const int st = u % kNS_O, dh = w >> 1, kh = w & 1;
-                        if (!(ok = mbar_wait_cluster(&bars->full[st], (u / kNS_O) & 1))) {
+                        if (!(ok = mbar_wait(&bars->full[st], (u / kNS_O) & 1))) {
                             set_timeout(p.status, kDiagPrefillPair, 1, 0, u);
                             break;
                         }
