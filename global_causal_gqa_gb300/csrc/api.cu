@@ -146,14 +146,16 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
                             float scale, const float *table, int table_len, int k_is_rotated,
                             void *workspace, size_t workspace_bytes, gqa_stream_t stream) {
     if (!q || !k || !v || !o || !table || B <= 0 || T <= 0 || S <= 0 || T > S || Hq <= 0 ||
-        Hkv <= 0 || (Hq % Hkv) != 0 || !(scale > 0.f) || !std::isfinite(scale))
+        Hkv <= 0 || (Hq % Hkv) != 0 || !(scale > 0.f) || !std::isfinite(scale) ||
+        k_is_rotated < 0 || k_is_rotated > 2)
         return GQA_ERR_INVALID_ARG;
     if (d != 128 && d != 256 && d != 512) return GQA_ERR_UNSUPPORTED;
+    if (k_is_rotated == 2 && d != 128) return GQA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(table) ||
         (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return GQA_ERR_ALIGNMENT;
     if (table_len < S) return GQA_ERR_RANGE;
-    if (!k_is_rotated) {
+    if (k_is_rotated == 0) {
         const size_t need = gqa_prefill_workspace_bytes(B, Hkv, S, d);
         if (!workspace || workspace_bytes < need) return GQA_ERR_WORKSPACE;
         if (!aligned16(workspace)) return GQA_ERR_ALIGNMENT;
@@ -171,14 +173,15 @@ gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o
     // K rotated once at positions 0..S-1 into the workspace; Q is rotated inside the
     // attention kernel as each tile lands.
     const void *k_rot = k;
-    if (!k_is_rotated) {
+    if (k_is_rotated == 0) {
         cudaError_t e = gqa::launch_rope_apply(k, workspace, static_cast<long>(B) * Hkv * S, S,
                                                d, 0, table, table_len, st, s);
         if (e != cudaSuccess) return GQA_ERR_CUDA;
         k_rot = workspace;
     }
     const int rc = d == 128 ? gqa::launch_prefill(q, k_rot, v, o, lse, B, T, S, Hq, Hkv, d,
-                                                  window, scale, table, table_len, st, s)
+                                                  window, scale, table, table_len, st, s,
+                                                  k_is_rotated == 2)
                             : gqa::launch_prefill_wide(q, k_rot, v, o, lse, B, T, S, Hq, Hkv,
                                                        d, window, scale, table, st, s);
     if (rc == GQA_ERR_CUDA) t_last_cuda_error = cudaGetLastError();

@@ -82,10 +82,12 @@ cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int
 size_t decode_workspace_bytes(int nseq, int Hq, int Hkv, int d, int max_len);
 
 // d = 128 prefill: picks the persistent kernel (prefill.cu) or the one-CTA-per-item
-// kernel (prefill_stream.cu) by the mean item length; returns a gqa_status
+// kernel (prefill_stream.cu) by the mean item length; returns a gqa_status.  fuse_k: K is
+// before RoPE and the persistent kernel rotates each K tile in shared memory.
 int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, float *lse,
                    int B, int T, int S, int Hq, int Hkv, int d, int window, float scale,
-                   const float *table, int table_len, int *status, cudaStream_t s);
+                   const float *table, int table_len, int *status, cudaStream_t s,
+                   bool fuse_k = false);
 
 // d = 128 prefill, one CTA per work item (prefill_stream.cu); returns a gqa_status
 int launch_prefill_stream(const void *q, const void *k_rot, const void *v, void *o, float *lse,

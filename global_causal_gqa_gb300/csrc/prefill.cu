@@ -26,10 +26,15 @@
 //               tiles into a 3-slot ring in the order the MMA thread consumes them:
 //               K(0), V(0), K(1), V(1), ...
 //   warp 1      tensor-memory allocator and the single MMA-issuing thread.
-//   warps 2-3   RoPE (§6.1) on each item's Q tiles in shared memory, ahead of use.
+//   warps 2-3   RoPE (§6.1) on each item's Q tiles in shared memory, ahead of use (and,
+//               in the fused-K form, on every K tile as it lands in the ring).
 //   warps 4-7   softmax + epilogue for query tile 0, warps 8-11 for query tile 1: one
 //               thread per query row; warp w reads TMEM lanes 32*(w%4).. (its quarter).
-// K arrives already rotated (the caller-side pass rotates each key once).
+// K normally arrives already rotated (the caller-side pass rotates each key once).  The
+// fused-K form (KROT) takes K before RoPE and rotates each K tile in shared memory, at
+// positions n0 .. n0 + 127, between its landing and its score products: no workspace and
+// no pass over K, but every reload of a K tile is rotated again (each tile is reloaded
+// once per query block whose window reaches it).
 //
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
 // P (bf16) overwrites the first 64 columns of its S tile and feeds the PV product
@@ -96,6 +101,7 @@ struct Bars {
     uint64_t s_full[2], p_full[2], o_done[2];     // per query tile
     uint64_t o_final[2];                          // an item's last PV product of the tile
     uint64_t o_free[2];                           // the epilogue has read O out of TMEM
+    uint64_t krot[2];                             // fused-K form: K tile rotated (alternate)
     uint64_t mma_done;
     uint32_t tmem_base;
 };
@@ -167,6 +173,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
 // Roles for the diagnostic code of an expired wait.
 enum Role { kRoleProducer = 0, kRoleMma = 1, kRoleSoftmax = 2, kRoleRope = 3 };
 
+template <bool KROT>   // K before RoPE, rotated tile by tile in shared memory
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_persistent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -200,6 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->clc_full[i], 1);
             mbar_init(&bars->item_free[i], kItemReaders);
         }
+        mbar_init(&bars->krot[0], kRotThreads);
+        mbar_init(&bars->krot[1], kRotThreads);
         mbar_init(&bars->mma_done, 1);
         fence_mbar_init();
     }
@@ -314,6 +323,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++u;
                 tc_fence_after();
             };
+            // a K tile: landed (or, fused-K form, rotated by warps 2-3: K tile kc of this
+            // CTA signals krot[kc & 1])
+            int kc = 0;
+            auto take_k = [&](int &st) {
+                if constexpr (!KROT) {
+                    take(st);
+                } else {
+                    st = u % kSlots;
+                    if (!(ok = mbar_wait(&bars->krot[kc & 1], (kc >> 1) & 1))) {
+                        set_timeout(p.status, kDiagPrefill, kRoleMma, 7, kc);
+                        return;
+                    }
+                    ++u;
+                    ++kc;
+                    tc_fence_after();
+                }
+            };
             auto issue_s = [&](uint32_t qaddr, int i, int st) {
                 const uint32_t ka = ring0 + st * kTileBytes;
 #pragma unroll
@@ -351,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 int kst = 0, vst = 0;
-                take(kst);
+                take_k(kst);
                 for (int i = 0; i < ntile && ok; ++i) {
                     // S_i(0) overwrites the columns the previous item's last P_i sits in
                     wait_last_pv(i, 2);
@@ -377,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         issue_pv(i, vst, j > 0);
                         if (j == n - 1) umma_commit(&bars->o_final[i]);
                         if (j + 1 < n) {
-                            if (i == 0) take(kst);
+                            if (i == 0) take_k(kst);
                             if (!ok) break;
                             // S_i(j+1) overwrites the columns P_i(j) sits in
                             wait_last_pv(i, 5);
@@ -404,10 +430,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp < 4) {
-        // ================= RoPE on Q tiles (warps 2-3) =================
+        // ================= RoPE on Q tiles (and fused-K K tiles), warps 2-3 =================
         // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7); the pair
         // (j, j + 64) is the same offset in box 0 and box 1
         const int rt = threadIdx.x - 64;   // 0..63
+        // rotates the 128 rows of a tile in shared memory, row r at position pos0 + r (rows
+        // at or past position S hold the load's zero fill and are left alone)
+        auto rotate_tile = [&](uint8_t *tile, int pos0) {
+            for (int rr = 0; rr < kBM / kRotThreads; ++rr) {
+                const int r = rt + kRotThreads * rr;
+                const int pos = pos0 + r;
+                if (pos >= p.S) continue;
+                const float4 *t4 = reinterpret_cast<const float4 *>(p.table + (size_t)pos * (kD / 2));
+                uint8_t *row0 = tile + r * 128;
+                uint8_t *row1 = row0 + kBoxBytes;
+#pragma unroll 2
+                for (int c = 0; c < 8; ++c) {
+                    const int pc = (c ^ (r & 7)) * 16;
+                    const uint4 a = *reinterpret_cast<uint4 *>(row0 + pc);
+                    const uint4 bq = *reinterpret_cast<uint4 *>(row1 + pc);
+                    float cs[16];
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const float4 tv = __ldg(t4 + 4 * c + qq);
+                        cs[4 * qq] = tv.x;
+                        cs[4 * qq + 1] = tv.y;
+                        cs[4 * qq + 2] = tv.z;
+                        cs[4 * qq + 3] = tv.w;
+                    }
+                    uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const float a0 = bf16lo(aw[qq]), a1 = bf16hi(aw[qq]);
+                        const float b0 = bf16lo(bw[qq]), b1 = bf16hi(bw[qq]);
+                        const float c0 = cs[4 * qq], s0 = cs[4 * qq + 1];
+                        const float c1 = cs[4 * qq + 2], s1 = cs[4 * qq + 3];
+                        aw[qq] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
+                        bw[qq] = pack_bf16x2(fmaf(a0, s0, b0 * c0), fmaf(a1, s1, b1 * c1));
+                    }
+                    *reinterpret_cast<uint4 *>(row0 + pc) = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+                    *reinterpret_cast<uint4 *>(row1 + pc) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+                }
+            }
+        };
+        int ku = 0;   // fused-K form: ring loads of the items so far
+        int kc = 0;   // fused-K form: K tiles rotated
         for (int k = 0, idx = blockIdx.x; idx >= 0; ++k) {
             const Item it = make_item(p, idx);
             const int buf = k & 1;
@@ -415,48 +482,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 set_timeout(p.status, kDiagPrefill, kRoleRope, 0, k);
                 break;
             }
-            for (int i = 0; i < (it.two ? 2 : 1); ++i) {
-                for (int rr = 0; rr < kBM / kRotThreads; ++rr) {
-                    const int r = rt + kRotThreads * rr;
-                    const int t = it.mb * kBM + r;
-                    if (t >= p.T) continue;
-                    const float4 *t4 = reinterpret_cast<const float4 *>(
-                        p.table + (size_t)(p.S - p.T + t) * (kD / 2));
-                    uint8_t *row0 = sQ(buf, i) + r * 128;
-                    uint8_t *row1 = row0 + kBoxBytes;
-#pragma unroll 2
-                    for (int c = 0; c < 8; ++c) {
-                        const int pc = (c ^ (r & 7)) * 16;
-                        const uint4 a = *reinterpret_cast<uint4 *>(row0 + pc);
-                        const uint4 bq = *reinterpret_cast<uint4 *>(row1 + pc);
-                        float cs[16];
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq) {
-                            const float4 tv = __ldg(t4 + 4 * c + qq);
-                            cs[4 * qq] = tv.x;
-                            cs[4 * qq + 1] = tv.y;
-                            cs[4 * qq + 2] = tv.z;
-                            cs[4 * qq + 3] = tv.w;
-                        }
-                        uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq) {
-                            const float a0 = bf16lo(aw[qq]), a1 = bf16hi(aw[qq]);
-                            const float b0 = bf16lo(bw[qq]), b1 = bf16hi(bw[qq]);
-                            const float c0 = cs[4 * qq], s0 = cs[4 * qq + 1];
-                            const float c1 = cs[4 * qq + 2], s1 = cs[4 * qq + 3];
-                            aw[qq] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
-                            bw[qq] = pack_bf16x2(fmaf(a0, s0, b0 * c0), fmaf(a1, s1, b1 * c1));
-                        }
-                        *reinterpret_cast<uint4 *>(row0 + pc) =
-                            make_uint4(aw[0], aw[1], aw[2], aw[3]);
-                        *reinterpret_cast<uint4 *>(row1 + pc) =
-                            make_uint4(bw[0], bw[1], bw[2], bw[3]);
-                    }
-                }
-            }
+            for (int i = 0; i < (it.two ? 2 : 1); ++i)
+                rotate_tile(sQ(buf, i), p.S - p.T + it.mb * kBM);
             fence_proxy_async_smem();
             mbar_arrive(&bars->q_ready[buf]);
+            if constexpr (KROT) {
+                // this item's K tiles, ring loads ku, ku + 2, ... (K and V alternate), each
+                // rotated at its keys' positions as soon as it lands
+                bool kok = true;
+                for (int j = 0; j < it.n_tiles; ++j) {
+                    const int u = ku + 2 * j, st = u % kSlots;
+                    if (!warp_wait(&bars->full[st], (u / kSlots) & 1)) {
+                        set_timeout(p.status, kDiagPrefill, kRoleRope, 2, kc);
+                        kok = false;
+                        break;
+                    }
+                    rotate_tile(smem + kSmemRing + st * kTileBytes, (it.kt_first + j) * kBN);
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars->krot[kc & 1]);
+                    ++kc;
+                }
+                ku += 2 * it.n_tiles;
+                if (!kok) break;
+            }
             bool ok = true;
             idx = __shfl_sync(0xffffffffu, read_item(bars, k + 1, p.n_items, ok), 0);
             if (!__all_sync(0xffffffffu, ok)) {
@@ -722,10 +770,10 @@ bool make_map(CUtensorMap *map, const void *base, int d, int rows, int slabs) {
 
 int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, float *lse, int B,
                    int T, int S, int Hq, int Hkv, int d, int window, float scale,
-                   const float *table, int table_len, int *status, cudaStream_t s) {
+                   const float *table, int table_len, int *status, cudaStream_t s, bool fuse_k) {
     (void)table_len;
     if (d != kD) return GQA_ERR_UNSUPPORTED;
-    {
+    if (!fuse_k) {
         // long items (a causal sweep over a long sequence): one CTA per item
         const int n_mb = (T + kBM - 1) / kBM;
         long tiles = 0;
@@ -742,8 +790,8 @@ int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, flo
     if (!make_map(&mq, q, d, T, B * Hq) || !make_map(&mk, k_rot, d, S, B * Hkv) ||
         !make_map(&mv, v, d, S, B * Hkv) || !make_map(&mo, o, d, T, B * Hq))
         return GQA_ERR_CUDA;
-    if (ensure_smem_attr(reinterpret_cast<const void *>(prefill_persistent_kernel),
-                         kSmemBytes) != cudaSuccess)
+    auto kern = fuse_k ? prefill_persistent_kernel<true> : prefill_persistent_kernel<false>;
+    if (ensure_smem_attr(reinterpret_cast<const void *>(kern), kSmemBytes) != cudaSuccess)
         return GQA_ERR_CUDA;   // the error stays readable with cudaGetLastError
     Params p;
     p.o = static_cast<__nv_bfloat16 *>(o);
@@ -763,8 +811,7 @@ int launch_prefill(const void *q, const void *k_rot, const void *v, void *o, flo
     if (n_items > 0x7fffffffL) return GQA_ERR_UNSUPPORTED;
     p.n_items = static_cast<int>(n_items);
     // one CTA per item; the CTAs that get an SM first claim the rest (cluster launch control)
-    prefill_persistent_kernel<<<static_cast<unsigned>(n_items), kThreads, kSmemBytes, s>>>(
-        mq, mk, mv, mo, p);
+    kern<<<static_cast<unsigned>(n_items), kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, p);
     const cudaError_t e = cudaPeekAtLastError();
     return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }

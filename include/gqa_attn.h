@@ -117,6 +117,11 @@ gqa_status gqa_rope_apply(const void *x, void *y, int B, int H, int T, int d, in
  *   gqa_prefill_workspace_bytes(B, Hkv, S, d) bytes; its contents are undefined afterwards.
  * k_is_rotated = 1: k already carries RoPE (a cache that stores rotated keys, as Gemma's
  *   does, §4.4); workspace may be NULL.
+ * k_is_rotated = 2 (d = 128 only, else GQA_ERR_UNSUPPORTED): k holds keys before RoPE and
+ *   each K tile is rotated in shared memory as it lands, inside the attention kernel (RoPE
+ *   fused into the tile load); workspace may be NULL.  Same results as 0, bit for bit.
+ *   Slower than 0 on long inputs: a K tile is rotated again every time a query block
+ *   reloads it, while 0 rotates each key once.  Any other value: GQA_ERR_INVALID_ARG.
  * Supports d = 128, 256, 512.  Hq % Hkv == 0. */
 size_t gqa_prefill_workspace_bytes(int B, int Hkv, int S, int d);
 gqa_status gqa_attn_prefill(const void *q, const void *k, const void *v, void *o,

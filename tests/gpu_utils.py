@@ -44,16 +44,18 @@ def oracle_freq(d: int, rope: RopeSpec) -> np.ndarray:
 
 
 def run_prefill(q, k, v, window: int, scale: float, table: torch.Tensor, table_len: int,
-                want_lse: bool = True):
-    """q/k/v on the GPU (bf16).  Returns (o, lse) from gqa_attn_prefill."""
+                want_lse: bool = True, k_mode: int = 0):
+    """q/k/v on the GPU (bf16), k before RoPE.  Returns (o, lse) from gqa_attn_prefill;
+    k_mode is its k_is_rotated argument: 0 rotates K once into a workspace, 2 rotates each
+    K tile inside the attention kernel."""
     B, Hq, T, d = q.shape
     _, Hkv, S, _ = k.shape
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device) if want_lse else None
-    wsb = gqa.gqa_prefill_workspace_bytes(B, Hkv, S, d)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=q.device)
+    wsb = gqa.gqa_prefill_workspace_bytes(B, Hkv, S, d) if k_mode == 0 else 0
+    ws = torch.empty(wsb, dtype=torch.uint8, device=q.device) if wsb else None
     gqa.gqa_attn_prefill(q, k, v, o, lse, B, T, S, Hq, Hkv, d, window, scale, table,
-                         table_len, 0, ws, wsb)
+                         table_len, k_mode, ws, wsb)
     st = gqa.gqa_get_device_status()
     assert st == 0, f"device status {gqa.STATUS_NAMES.get(st, st)}"
     return o, lse

@@ -126,6 +126,20 @@ def test_bad_arguments_rejected_on_host():
     assert gqa.gqa_status_string(-6) == "device-side wait timed out"
 
 
+def test_k_rotation_modes_checked_on_host():
+    """k_is_rotated: 0 (rotate once into the workspace), 1 (already rotated), 2 (rotated in
+    the tile load, d = 128 only); anything else is rejected before any launch."""
+    L = gqa.lib()
+    S = gqa.STATUS_NAMES
+    fake = 0x10000
+    for bad in (-1, 3, 7):
+        assert S[L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 2, 1, 128, 0, 0.1,
+                                    fake, 8, bad, None, 0, None)] == "GQA_ERR_INVALID_ARG"
+    for d in (256, 512):
+        assert S[L.gqa_attn_prefill(fake, fake, fake, fake, None, 1, 8, 8, 2, 1, d, 0, 0.1,
+                                    fake, 8, 2, None, 0, None)] == "GQA_ERR_UNSUPPORTED"
+
+
 def test_watchdog_selftest_limits_rejected_on_host():
     L = gqa.lib()
     S = gqa.STATUS_NAMES

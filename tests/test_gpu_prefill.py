@@ -203,3 +203,46 @@ def test_wide_single_tile_items():
 def test_wide_long_causal_sampled():
     """d = 256 causal sweep over 97 query blocks of up to 97 key tiles each."""
     _sampled_case(_layer(1, 12400, 12400, 2, 1, 0, d=256, seed=85), 1024, 9)
+
+
+# ---- RoPE on K fused into the tile load (k_is_rotated = 2, d = 128) ----
+FUSED_CASES = [
+    _layer(1, 200, 200, 2, 1, 0, seed=91),
+    _layer(1, 300, 300, 4, 1, 4, seed=92),
+    _layer(1, 384, 384, 2, 1, 129, seed=93),
+    _layer(2, 257, 257, 6, 2, 64, YARN, seed=94),
+    _layer(1, 160, 160, 3, 1, 0, seed=95),
+    _layer(1, 129, 700, 4, 2, 200, YARN, seed=96),
+    _layer(1, 2000, 2000, 16, 2, 0, seed=97),   # long causal items: still the fused kernel
+]
+
+
+@pytest.mark.parametrize("layer", FUSED_CASES, ids=lambda l: l.label)
+def test_fused_k_rope_equals_rotate_once(layer):
+    """K's rotation fused into the tile load gives the rotate-once result bit for bit (the
+    same fp32 rotation of the same bf16 keys, rounded once), and matches the oracle."""
+    gu.require_gpu()
+    x = prefill_inputs(layer)
+    q, k, v = gu.to_cuda(x.q, x.k, x.v)
+    table = gu.rope_table(layer.d, layer.rope, layer.S)
+    o0, l0 = gu.run_prefill(q, k, v, layer.window, layer.scale, table, layer.S, k_mode=0)
+    o2, l2 = gu.run_prefill(q, k, v, layer.window, layer.scale, table, layer.S, k_mode=2)
+    assert torch.equal(o0, o2) and torch.equal(l0, l2)
+    w = gu.oracle_freq(layer.d, layer.rope)
+    ro, rl = gu.orc().attention(x.q, x.k, x.v, window=layer.window, scale=layer.scale, w=w,
+                                amp=layer.rope.amp)
+    gu.compare(o2, ro, what=layer.label + " fused K")
+    gu.compare(l2, rl, what=layer.label + " fused K lse")
+
+
+def test_fused_k_rope_full_size_local_layer():
+    """The PLaMo-3-shaped local layer (B=2, T=S=8192, 64/8 heads, W=2048) with the fused
+    form: equal to the rotate-once result bit for bit."""
+    gu.require_gpu()
+    layer = WORKLOADS["plamo3_local_prefill"].layers[0]
+    x = prefill_inputs(layer)
+    q, k, v = gu.to_cuda(x.q, x.k, x.v)
+    table = gu.rope_table(layer.d, layer.rope, layer.S)
+    o0, l0 = gu.run_prefill(q, k, v, layer.window, layer.scale, table, layer.S, k_mode=0)
+    o2, l2 = gu.run_prefill(q, k, v, layer.window, layer.scale, table, layer.S, k_mode=2)
+    assert torch.equal(o0, o2) and torch.equal(l0, l2)
