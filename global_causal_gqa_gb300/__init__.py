@@ -33,7 +33,7 @@ GQA_OK = 0
 STATUS_NAMES = {
     0: "GQA_OK", -1: "GQA_ERR_INVALID_ARG", -2: "GQA_ERR_UNSUPPORTED", -3: "GQA_ERR_ALIGNMENT",
     -4: "GQA_ERR_CAPACITY", -5: "GQA_ERR_CUDA", -6: "GQA_ERR_DEVICE_TIMEOUT",
-    -7: "GQA_ERR_WORKSPACE", -8: "GQA_ERR_RANGE",
+    -7: "GQA_ERR_WORKSPACE", -8: "GQA_ERR_RANGE", -9: "GQA_ERR_DEVICE_BOUNDS",
 }
 
 

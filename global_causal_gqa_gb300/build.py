@@ -4,6 +4,11 @@ Each translation unit is compiled in parallel with `-gencode arch=compute_103a,
 code=sm_103a -lineinfo -O3`, then linked with `nvcc -shared` (static CUDA runtime, so
 the library loads on a machine without a GPU and needs no libcuda at link time).
 Extra nvcc flags may be given in the GQA_NVCC_FLAGS environment variable.
+
+`build(debug=True)` makes a second library, libgqa_attn_debug.so (objects in _build_debug),
+compiled with -DGQA_DEBUG_BOUNDS: every global access whose index comes from device-side
+data is checked first, and a failed check records GQA_ERR_DEVICE_BOUNDS instead of
+accessing memory.  It is slower and meant for testing; the normal library has no checks.
 """
 from __future__ import annotations
 
@@ -19,6 +24,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgqa_attn.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libgqa_attn_debug.so")
 SOURCES = ["api.cu", "rope.cu", "kv.cu", "decode.cu", "prefill.cu", "prefill_stream.cu",
            "prefill_wide.cu", "prefill_pair.cu", "qknorm.cu", "chunk.cu", "watchdog.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
@@ -41,18 +48,21 @@ def _newest_input() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def up_to_date() -> bool:
-    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input()
+def up_to_date(lib: str = LIB) -> bool:
+    return os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if debug:
+        extra_flags = (*extra_flags, "-DGQA_DEBUG_BOUNDS")
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(bdir, os.path.splitext(src)[0] + ".o")
         env_flags = os.environ.get("GQA_NVCC_FLAGS", "").split()
         cmd = [cc, *ARCH, *FLAGS, *extra_flags, *env_flags, "-c", os.path.join(CSRC, src),
                "-o", obj]
@@ -67,13 +77,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

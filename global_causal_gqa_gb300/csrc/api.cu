@@ -457,6 +457,7 @@ const char *gqa_status_string(int status) {
         case GQA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
         case GQA_ERR_WORKSPACE: return "workspace missing or too small";
         case GQA_ERR_RANGE: return "position beyond the RoPE table";
+        case GQA_ERR_DEVICE_BOUNDS: return "device-side index check failed (debug build)";
         default: return "unknown status";
     }
 }

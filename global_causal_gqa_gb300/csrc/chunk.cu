@@ -78,12 +78,14 @@ __global__ void prefill_gather_kernel(const gqa_kv_desc *__restrict__ desc_p,
         if (r < R) {
             int slot = first + r;
             if (slot >= cap) slot -= cap;
+            if (!GQA_IN_BOUNDS(slot, cap, status, (kDiagCache << 24) | 3)) continue;
             ks = kc + ((long)h * cap + slot) * rc;
             vs = vc + ((long)h * cap + slot) * rc;
         } else {
             ks = k_new + ((long)h * T + (r - R)) * rc;
             vs = v_new + ((long)h * T + (r - R)) * rc;
         }
+        if (!GQA_IN_BOUNDS(r, table_len, status, (kDiagCache << 24) | 4)) continue;
         uint4 a = ks[c], b = ks[c + cpr];
         rotate_pairs(a, b, table + ((long)r * (d / 2) + 8 * c) / 2);
         uint4 *ko = k_out + ((long)h * S + r) * rc;
@@ -121,6 +123,7 @@ __global__ void kv_append_chunk_kernel(gqa_kv_desc *descs, const uint4 *__restri
             const long ht = i / rc;
             const int t = t0 + static_cast<int>(ht % (T - t0)), h = static_cast<int>(ht / (T - t0));
             const long slot = ring ? ((long)count + t) % cap : (long)count + t;
+            if (!GQA_IN_BOUNDS(slot, cap, status, (kDiagCache << 24) | 5)) continue;
             const long src = (((long)seq * Hkv + h) * T + t) * rc + c;
             const long dst = ((long)h * cap + slot) * rc + c;
             kc[dst] = k_new[src];

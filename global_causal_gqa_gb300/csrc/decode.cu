@@ -257,7 +257,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     uint32_t qb[8][2];
     {
         uint4 qc[4];
-        if (gq < G) {
+        if (gq < G && GQA_IN_BOUNDS((size_t)seq * Hq + (size_t)g * G + gq,
+                                    (size_t)gridDim.y * Hq, status, (kDiagDecode << 24) | 1) &&
+            GQA_IN_BOUNDS(qpos, desc.rope_len, status, (kDiagDecode << 24) | 5)) {
             const uint4 *qr = reinterpret_cast<const uint4 *>(
                 q + ((size_t)seq * Hq + (size_t)g * G + gq) * d);
 #pragma unroll
@@ -307,7 +309,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         SHARED ? kbase : static_cast<const __nv_bfloat16 *>(desc.v) + (size_t)g * sv.cap * d;
     auto slot_of = [&](int key) {
         int s = sv.first + key;
-        return s >= sv.cap ? s - sv.cap : s;
+        s = s >= sv.cap ? s - sv.cap : s;
+        if (!GQA_IN_BOUNDS(s, sv.cap, status, (kDiagDecode << 24) | 2)) s = 0;
+        return s;
     };
 
     // One block = 16 keys: K rows kb + gq and kb + gq + 8, V rows kb + 2tq + {0, 1, 8, 9}
@@ -353,7 +357,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                     reinterpret_cast<const float4 *>(table + pb(lane >> 4)) + (lane & 15);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int row = min(kb + i, k_end - 1);
+                    int row = min(kb + i, k_end - 1);
+                    if (!GQA_IN_BOUNDS(row, desc.rope_len, status, (kDiagDecode << 24) | 4)) row = 0;
                     const int k = ((i >> 3) << 3) | kq;
                     const int lp = ((i & 7) << 2) | lp_lo;
                     cp_async16(stg + k * 32 + (lp ^ ((k & 3) << 1)), src + (size_t)row * (d / 4));
@@ -362,7 +367,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const int row = min(kb + i, k_end - 1);
+                int row = min(kb + i, k_end - 1);
+                if (!GQA_IN_BOUNDS(row, desc.rope_len, status, (kDiagDecode << 24) | 4)) row = 0;
                 const int k = ((i >> 3) << 3) | kq;
                 const int lp = ((i & 7) << 2) | lp_lo;
                 cp_async16(stg + k * 32 + (lp ^ ((k & 3) << 1)),
@@ -531,6 +537,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const int h0 = 2 * tq, h1 = 2 * tq + 1;  // heads within the group
     const size_t rec0 = ((size_t)seq * Hq + (size_t)g * G + h0) * nsplit + split;
     const size_t rec1 = ((size_t)seq * Hq + (size_t)g * G + h1) * nsplit + split;
+    const size_t n_rec = (size_t)gridDim.y * Hq * nsplit;   // partial records in the workspace
+    const bool rec0_ok = h0 >= G || GQA_IN_BOUNDS(rec0, n_rec, status, (kDiagDecode << 24) | 6);
+    const bool rec1_ok = h1 >= G || GQA_IN_BOUNDS(rec1, n_rec, status, (kDiagDecode << 24) | 6);
     // this warp's output elements: local 64 (i >> 1) + 8 gq + 4 (i & 1) + 0..3, i.e.
     // global 64 part + 8 gq + ... in the first half and d/2 + 64 part + ... in the second
     auto out_off = [&](int i) {
@@ -557,7 +566,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             out1[c] = par ? make_float4(r2, hi[1], r3, hi[3]) : make_float4(lo[1], r2, lo[3], r3);
         }
         auto sh_off = [&](int c) { return 8 * gchunk(4 * c + (gq >> 1)) + 4 * par; };
-        if (h0 < G) {
+        if (h0 < G && rec0_ok) {
             if (gq == 0 && part == 0) {
                 ws_ml[2 * rec0] = m_run0;
                 ws_ml[2 * rec0 + 1] = l_run0;
@@ -566,7 +575,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             for (int c = 0; c < 4; ++c)
                 *reinterpret_cast<float4 *>(ws_o + rec0 * d + sh_off(c)) = out0[c];
         }
-        if (h1 < G) {
+        if (h1 < G && rec1_ok) {
             if (gq == 0 && part == 0) {
                 ws_ml[2 * rec1] = m_run1;
                 ws_ml[2 * rec1 + 1] = l_run1;
@@ -577,7 +586,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         }
         return;
     }
-    if (h0 < G) {
+    if (h0 < G && rec0_ok) {
         if (gq == 0 && part == 0) {
             ws_ml[2 * rec0] = m_run0;
             ws_ml[2 * rec0 + 1] = l_run0;
@@ -587,7 +596,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             *reinterpret_cast<float4 *>(ws_o + rec0 * d + out_off(i)) =
                 make_float4(o[2 * i][0], o[2 * i][2], o[2 * i + 1][0], o[2 * i + 1][2]);
     }
-    if (h1 < G) {
+    if (h1 < G && rec1_ok) {
         if (gq == 0 && part == 0) {
             ws_ml[2 * rec1] = m_run1;
             ws_ml[2 * rec1 + 1] = l_run1;
@@ -604,14 +613,15 @@ __global__ void __launch_bounds__(kMaxHeadDim)
     decode_combine_kernel(const gqa_kv_desc *__restrict__ descs, int Hq, int d, int max_len,
                           int chunk, int nsplit, const float *__restrict__ ws_ml,
                           const float *__restrict__ ws_o, __nv_bfloat16 *__restrict__ out,
-                          float *__restrict__ lse) {
+                          float *__restrict__ lse, int *status) {
     const int h = blockIdx.x, seq = blockIdx.y, dd = threadIdx.x;
     griddep_wait();               // this step's partials
     griddep_launch_dependents();
     const SeqView sv = seq_view(descs[seq], max_len);
     if (!sv.ok) return;
-    const int ns = (sv.R + chunk - 1) / chunk;
+    int ns = (sv.R + chunk - 1) / chunk;
     const size_t rec = ((size_t)seq * Hq + h) * nsplit;
+    if (!GQA_IN_BOUNDS(ns - 1, nsplit, status, (kDiagDecode << 24) | 7)) ns = 0;
     float M = -CUDART_INF_F;
     for (int s = 0; s < ns; ++s) M = fmaxf(M, ws_ml[2 * (rec + s)]);
     float L = 0.f, acc = 0.f;
@@ -679,7 +689,8 @@ cudaError_t launch_decode(const void *q, const gqa_kv_desc *descs, int nseq, int
     if (e != cudaSuccess) return e;
     return launch_pdl(decode_combine_kernel, dim3(Hq, nseq), dim3(d), 0, s, descs, Hq, d,
                       max_len, sp.chunk, nsplit, static_cast<const float *>(ws_ml),
-                      static_cast<const float *>(ws_o), static_cast<__nv_bfloat16 *>(o), lse);
+                      static_cast<const float *>(ws_o), static_cast<__nv_bfloat16 *>(o), lse,
+                      status);
 }
 
 }  // namespace gqa

@@ -34,7 +34,7 @@ __global__ void kv_append_kernel(gqa_kv_desc *descs, const uint4 *__restrict__ k
     }
     __syncthreads();
     const int slot = s_slot;
-    if (slot >= 0) {
+    if (slot >= 0 && GQA_IN_BOUNDS(slot, desc->cap, status, (kDiagCache << 24) | 1)) {
         const int cpr = d / 8;  // 16-byte chunks per row
         const long cap = desc->cap;
         uint4 *kc = static_cast<uint4 *>(desc->k);

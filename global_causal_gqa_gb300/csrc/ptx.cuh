@@ -36,7 +36,8 @@ enum DiagKernel {
     kDiagPrefillWide = 2,
     kDiagDecode = 3,
     kDiagWatchdog = 4,
-    kDiagPrefillPair = 5
+    kDiagPrefillPair = 5,
+    kDiagCache = 6   // cache append, chunk gather, RoPE pass, Q/K normalisation
 };
 __device__ __forceinline__ void set_timeout(int *status, int kernel, int role, int barrier,
                                             int tile) {
@@ -46,6 +47,28 @@ __device__ __forceinline__ void set_timeout(int *status, int kernel, int role, i
     atomicCAS(status + 1, 0, code);                // first expired wait overall
     atomicCAS(status + 2 + (role & 3), 0, code);   // first expired wait of this role
 }
+
+// ---- index checks of the debug build ----------------------------------------------------
+// Built with -DGQA_DEBUG_BOUNDS, GQA_IN_BOUNDS(i, n, status, site) checks 0 <= i < n before
+// a global access whose index comes from device-side data (a cache slot, a table row, a
+// workspace record).  A failing check records GQA_ERR_DEVICE_BOUNDS (the first device
+// error wins) and the site's code in the diagnostic word, (kernel << 24) | (1 << 23) |
+// site, and evaluates to false: the caller skips the access or uses a safe index.  It
+// never traps.  In other builds it is the constant true.
+#ifdef GQA_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds(long i, long n, int *status, int site) {
+    if (i >= 0 && i < n) return true;
+    if (status) {
+        atomicCAS(status, 0, -9 /* GQA_ERR_DEVICE_BOUNDS */);
+        atomicCAS(status + 1, 0, site | (1 << 23));
+    }
+    return false;
+}
+#define GQA_IN_BOUNDS(i, n, status, site) \
+    ::gqa::in_bounds(static_cast<long>(i), static_cast<long>(n), (status), (site))
+#else
+#define GQA_IN_BOUNDS(i, n, status, site) true
+#endif
 
 // ---- mbarrier ---------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(256) qk_norm_append_kernel(
             const float ss = warp_sum(load_row(q + src, d, lane, row));
             finish_row(row, d, lane, rsqrtf(ss / d + eps), q_gamma, q_out + src, nullptr,
                        nullptr);
-        } else if (slot >= 0) {
+        } else if (slot >= 0 && GQA_IN_BOUNDS(slot, cap, status, (kDiagCache << 24) | 2)) {
             const bool is_k = r < Hq + Hkv;
             const int g = is_k ? r - Hq : r - Hq - Hkv;
             const long src = ((long)seq * Hkv + g) * wpr;

@@ -62,7 +62,8 @@ typedef enum gqa_status {
     GQA_ERR_CUDA = -5,            /* a CUDA runtime call failed */
     GQA_ERR_DEVICE_TIMEOUT = -6,  /* a device-side bounded wait expired */
     GQA_ERR_WORKSPACE = -7,       /* workspace missing or too small */
-    GQA_ERR_RANGE = -8            /* a position lies beyond the RoPE table */
+    GQA_ERR_RANGE = -8,           /* a position lies beyond the RoPE table */
+    GQA_ERR_DEVICE_BOUNDS = -9    /* debug build only: a device-side index check failed */
 } gqa_status;
 
 /* ---- RoPE frequencies and table ---------------------------------------------------
@@ -308,8 +309,12 @@ gqa_status gqa_get_device_status(gqa_stream_t stream);
  * first overall, diag[1..4] the first of each kernel role 0..3.  A code is
  * (kernel << 24) | (role << 20) | (barrier << 16) | (tile index & 0xffff), kernel 1 =
  * prefill d=128, 2 = prefill d=256, 3 = decode, 4 = gqa_watchdog_selftest,
- * 5 = prefill d=512 (a pair of CTAs).  For
- * diagnosing GQA_ERR_DEVICE_TIMEOUT; gqa_get_device_status leaves the codes in place. */
+ * 5 = prefill d=512 (a pair of CTAs), 6 = cache append, chunk gather, RoPE pass, Q/K
+ * normalisation.  A library compiled with -DGQA_DEBUG_BOUNDS checks the indices of the
+ * global accesses it derives from device-side data; the first failed check records
+ * GQA_ERR_DEVICE_BOUNDS and, in diag[0], (kernel << 24) | (1 << 23) | site, and the access
+ * is skipped.  For diagnosing device-side errors; gqa_get_device_status leaves the codes
+ * in place. */
 gqa_status gqa_get_device_diag(gqa_stream_t stream, int32_t *diag, int n);
 
 /* Self-test of the device-side watchdog (the pages have no counterpart: this checks the
