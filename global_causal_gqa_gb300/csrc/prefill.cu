@@ -23,11 +23,12 @@
 // Warp roles (12 warps, 3 warpgroups; 3 warps per SM sub-partition cap every thread at
 // 168 registers):
 //   warp 0      TMA producer: Q tiles of each item into Q buffer (item & 1), K and V
-//               tiles into a 3-slot ring in the order the MMA thread consumes them:
+//               tiles into a 3-slot ring in the order they are consumed:
 //               K(0), V(0), K(1), V(1), ...
 //   warp 1      tensor-memory allocator and the single MMA-issuing thread.
 //   warps 2-3   RoPE (§6.1) on each item's Q tiles in shared memory, ahead of use (and,
-//               in the fused-K form, on every K tile as it lands in the ring).
+//               in the fused-K form, on every K tile as it lands in the ring); warp 2 also
+//               issues the TMA stores of each item's O once the epilogue has staged it.
 //   warps 4-7   softmax + epilogue for query tile 0, warps 8-11 for query tile 1: one
 //               thread per query row; warp w reads TMEM lanes 32*(w%4).. (its quarter).
 // K normally arrives already rotated (the caller-side pass rotates each key once).  The
@@ -96,7 +97,7 @@ struct Bars {
     uint64_t item_free[kItemSlots];               // every role has read that response
     uint64_t q_full[2], q_ready[2];               // per Q buffer
     uint64_t epi_done[2];                         // the buffer's O staging has been stored
-    uint64_t staged[2];                           // per query tile: O rows written to smem
+    uint64_t staged[2][2];                        // [buffer][query tile]: O rows in smem
     uint64_t full[kSlots], empty[kSlots];         // K/V ring
     uint64_t s_full[2], p_full[2], o_done[2];     // per query tile
     uint64_t o_final[2];                          // an item's last PV product of the tile
@@ -192,7 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->q_full[i], 1);
             mbar_init(&bars->q_ready[i], kRotThreads);
             mbar_init(&bars->epi_done[i], 2);
-            mbar_init(&bars->staged[i], 128);
+            mbar_init(&bars->staged[i][0], 128);
+            mbar_init(&bars->staged[i][1], 128);
             mbar_init(&bars->s_full[i], 1);
             mbar_init(&bars->p_full[i], 128);
             mbar_init(&bars->o_done[i], 1);
@@ -221,6 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
+    // Register split (launch: 384 threads x 168): the producer, MMA and RoPE warps
+    // (warpgroup 0) give registers to the two softmax warpgroups, which hold a whole
+    // 128-column S row per thread: 128 x 96 + 256 x 200 <= 384 x 168, and neither side
+    // spills.
+    if (warp < 4) {
+    reg_dealloc<96>();
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
@@ -385,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 umma_commit(&bars->empty[kst]);
+                int kprev = kst;   // K slot of the last score products issued
                 for (int j = 0; j < n && ok; ++j) {
                     take(vst);
                     for (int i = 0; i < ntile && ok; ++i) {
@@ -402,6 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         issue_pv(i, vst, j > 0);
                         if (j == n - 1) umma_commit(&bars->o_final[i]);
+                        // slots whose last reader has been issued, released here rather
+                        // than between a score product and the next PV product: K(j)
+                        // (read by S_1(j), issued in the previous step) and V(j)
+                        if (i == 0 && j > 0) umma_commit(&bars->empty[kprev]);
+                        if (i == ntile - 1) umma_commit(&bars->empty[vst]);
                         if (j + 1 < n) {
                             if (i == 0) take_k(kst);
                             if (!ok) break;
@@ -410,9 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (ok) issue_s(qaddr[i], i, kst);
                         }
                     }
-                    if (!ok) break;
-                    umma_commit(&bars->empty[vst]);
-                    if (j + 1 < n) umma_commit(&bars->empty[kst]);
+                    kprev = kst;
                 }
                 if (!ok) break;
                 for (int i = 0; i < ntile; ++i) ++nepi[i];
@@ -430,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp < 4) {
-        // ================= RoPE on Q tiles (and fused-K K tiles), warps 2-3 =================
+        // ================= RoPE on Q tiles (and fused-K K tiles); O stores =================
         // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7); the pair
         // (j, j + 64) is the same offset in box 0 and box 1
         const int rt = threadIdx.x - 64;   // 0..63
@@ -475,11 +487,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         int ku = 0;   // fused-K form: ring loads of the items so far
         int kc = 0;   // fused-K form: K tiles rotated
-        for (int k = 0, idx = blockIdx.x; idx >= 0; ++k) {
+        int nst[2][2] = {{0, 0}, {0, 0}};   // staged completions consumed, [buffer][tile]
+        // stores item kk's O (the plain form; the fused-K form stores from the epilogue):
+        // waits until the epilogue has staged its tiles in Q buffer kk & 1, one TMA store
+        // per 64-column box, and frees the buffer once the stores have read it
+        auto store_o = [&](int kk, const Item &itp) {
+            const int nt = itp.two ? 2 : 1;
+            for (int t = 0; t < nt; ++t) {
+                if (!warp_wait(&bars->staged[kk & 1][t], nst[kk & 1][t] & 1)) {
+                    set_timeout(p.status, kDiagPrefill, kRoleRope, 3, kk);
+                    return false;
+                }
+                ++nst[kk & 1][t];
+            }
+            if (lane == 0) {
+                for (int t = 0; t < nt; ++t) {
+                    const int zo = itp.b * p.Hq + itp.h0 + t;
+                    tma_store_3d(&tmO, sQ(kk & 1, t), 0, itp.mb * kBM, zo);
+                    tma_store_3d(&tmO, sQ(kk & 1, t) + kBoxBytes, 64, itp.mb * kBM, zo);
+                }
+                bulk_commit_group();
+                bulk_wait_read_all();
+                mbar_arrive_cnt(&bars->epi_done[kk & 1], 2);
+            }
+            __syncwarp();
+            return true;
+        };
+        Item prev{};
+        int k = 0;
+        bool rok = true;
+        for (int idx = blockIdx.x; rok && idx >= 0; ++k) {
             const Item it = make_item(p, idx);
             const int buf = k & 1;
             if (!warp_wait(&bars->q_full[buf], (k >> 1) & 1)) {
                 set_timeout(p.status, kDiagPrefill, kRoleRope, 0, k);
+                rok = false;
                 break;
             }
             for (int i = 0; i < (it.two ? 2 : 1); ++i)
@@ -489,12 +531,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (KROT) {
                 // this item's K tiles, ring loads ku, ku + 2, ... (K and V alternate), each
                 // rotated at its keys' positions as soon as it lands
-                bool kok = true;
                 for (int j = 0; j < it.n_tiles; ++j) {
                     const int u = ku + 2 * j, st = u % kSlots;
                     if (!warp_wait(&bars->full[st], (u / kSlots) & 1)) {
                         set_timeout(p.status, kDiagPrefill, kRoleRope, 2, kc);
-                        kok = false;
+                        rok = false;
                         break;
                     }
                     rotate_tile(smem + kSmemRing + st * kTileBytes, (it.kt_first + j) * kBN);
@@ -503,18 +544,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++kc;
                 }
                 ku += 2 * it.n_tiles;
-                if (!kok) break;
+                if (!rok) break;
+            } else if (warp == 2 && k >= 1 && !(rok = store_o(k - 1, prev))) {
+                break;
             }
-            bool ok = true;
-            idx = __shfl_sync(0xffffffffu, read_item(bars, k + 1, p.n_items, ok), 0);
-            if (!__all_sync(0xffffffffu, ok)) {
+            prev = it;
+            idx = __shfl_sync(0xffffffffu, read_item(bars, k + 1, p.n_items, rok), 0);
+            if (!__all_sync(0xffffffffu, rok)) {
                 set_timeout(p.status, kDiagPrefill, kRoleRope, 1, k + 1);
+                rok = false;
                 break;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->item_free[item_slot(k + 1)]);
         }
+        // the last item's O; every store completes before the CTA exits
+        if (!KROT && warp == 2 && rok && k >= 1) store_o(k - 1, prev);
+        if (warp == 2 && lane == 0) bulk_wait_all();
+    }
     } else {
+        reg_alloc<200>();
         // ================= softmax / epilogue =================
         const int wg = (warp - 4) >> 2;      // query tile
         const int r = (warp & 3) * 32 + lane;  // row in tile == TMEM lane
@@ -524,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int cs = 0;    // score tiles consumed (all items)
         int pvb = 0;   // PV products of the previous items
         int ne = 0;    // items finished
+        int nsb[2] = {0, 0};   // items finished per Q buffer
         bool ok = true;
         for (int k = 0, idx = blockIdx.x; ok && idx >= 0; ++k) {
             // the item after this one (read at the end of the loop body)
@@ -694,10 +744,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    pack_bf16x2(x[8 * c + 6] * inv_l, x[8 * c + 7] * inv_l));
             }
             fence_proxy_async_smem();
-            mbar_arrive(&bars->staged[wg]);
+            mbar_arrive(&bars->staged[k & 1][wg]);
             const Item it = make_item(p, idx);
-            if (r == 0) {
-                if (!mbar_wait(&bars->staged[wg], ne & 1)) {
+            if (KROT && r == 0) {
+                // fused-K form: the RoPE warp is busy with K tiles, the epilogue stores
+                if (!mbar_wait(&bars->staged[k & 1][wg], nsb[k & 1] & 1)) {
                     set_timeout(p.status, kDiagPrefill, kRoleSoftmax, 3, ne);
                     ok = false;
                 } else {
@@ -712,6 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             ++ne;
+            ++nsb[k & 1];
             if (valid && p.lse) {
                 const int t = it.mb * kBM + r;
                 p.lse[((size_t)it.b * p.Hq + it.h0 + wg) * p.T + t] =
