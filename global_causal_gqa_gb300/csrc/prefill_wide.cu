@@ -365,6 +365,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 c_hi = valid ? min(BN, qpos - n0 + 1) : 0;
                 c_lo = p.window > 0 ? max(0, qpos - p.window + 1 - n0) : 0;
             }
+            // Masking, decided per warp and 32-column chunk, applied in tensor memory
+            // before the row is loaded: a chunk visible in all 32 rows of the warp is left
+            // alone; one hidden in all of them gets -inf and is skipped below (P = 0, no
+            // exponentials); a mixed one is masked element by element.  The chunk loop is
+            // not unrolled (one copy of the code, taken on the window-edge and diagonal
+            // tiles only).
+            uint32_t dead = 0;   // chunks hidden in every row of the warp
+            if (!__all_sync(0xffffffffu, full)) {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    const bool vis = c_lo <= 32 * c && 32 * c + 32 <= c_hi;
+                    const bool hid = c_hi <= 32 * c || 32 * c + 32 <= c_lo || c_hi <= c_lo;
+                    if (__all_sync(0xffffffffu, vis)) continue;
+                    uint32_t rr[32];
+                    if (__all_sync(0xffffffffu, hid)) {
+                        dead |= 1u << c;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(-CUDART_INF_F);
+                    } else {
+                        tmem_ld32(tS + 32 * c, rr);
+                        tmem_wait_ld();
+                        const int lo = c_lo - 32 * c, hi = c_hi - 32 * c;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (i < lo || i >= hi) rr[i] = __float_as_uint(-CUDART_INF_F);
+                    }
+                    tmem_st32(tS + 32 * c, rr);
+                }
+                tmem_wait_st();
+            }
             float x[BN];
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
@@ -374,10 +404,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(rr[i]);
             }
             tmem_wait_ld();
-            if (!full) {
-#pragma unroll
-                for (int i = 0; i < BN; ++i) x[i] = (i >= c_lo && i < c_hi) ? x[i] : -CUDART_INF_F;
-            }
             constexpr int CH = BN / 8;   // values per max chain
             float mx8[8];
 #pragma unroll
@@ -402,6 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t pk[16];
+                if (dead & (1u << c)) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                    tmem_st16(tS + 16 * c, pk);
+                    continue;
+                }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float2 a = ffma2(make_float2(x[32 * c + 2 * i], x[32 * c + 2 * i + 1]),
