@@ -25,8 +25,9 @@
 //
 // Shared K/V projection (Gemma 4 global layers, attention_k_eq_v, §5.2 and §8 of the same
 // page): the cache holds one row Zn = N_1(Z) per token; the values are Zn and the keys
-// RoPE(gamma_k * Zn), the fp32 gain multiplied into each loaded K element in fp32 and
-// rotated in fp32, with one rounding to bf16 for the MMA.  Each row is loaded once, in the
+// RoPE(gamma_k * Zn), the fp32 gain multiplied into each loaded K element of a rotating
+// pair in fp32 and rotated in fp32, with one rounding to bf16 for the MMA (pairs that
+// never rotate carry the gain on the query instead).  Each row is loaded once, in the
 // K layout; the V fragments are the 8x8 transposes (movmatrix) of those registers taken
 // before the gain and the rotation, so every byte of the cache crosses L1 once: half the
 // traffic of separate K and V.
@@ -110,13 +111,6 @@ __device__ __forceinline__ void gain_rotate_word(uint4 &a, uint4 &b, int q, cons
     const float2 rb = ffma2v(av, s, fmul2(bv, c));
     aw = pack_bf16x2(ra.x, ra.y);
     bw = pack_bf16x2(rb.x, rb.y);
-}
-
-// The same for pairs that never rotate (p-RoPE): the gain alone, one rounding.
-__device__ __forceinline__ void gain_word(uint4 &a, int q, const float2 &g) {
-    uint32_t &aw = q == 0 ? a.x : q == 1 ? a.y : q == 2 ? a.z : a.w;
-    const float2 v = fmul2(make_float2(bf16lo(aw), bf16hi(aw)), g);
-    aw = pack_bf16x2(v.x, v.y);
 }
 
 // Gain pair qq (elements 2 qq, 2 qq + 1) of a chunk whose 8 gains are g[0], g[1].
@@ -288,6 +282,28 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         const unsigned b = __ballot_sync(0xffffffffu, id);
         rot0 = (b & 0xFFFFu) != 0xFFFFu;
         rot1 = (b >> 16) != 0xFFFFu;
+        if constexpr (SHARED) {
+            // A group of pairs that never rotates takes the key gain on the query instead:
+            // sum_e q_e (gamma_e z_e) = sum_e (gamma_e q_e) z_e, so its keys are the raw
+            // rows and the per-key gain work is gone; gamma_e q_e is formed in fp32 and
+            // rounded once, as gamma_e z_e is for the rotating pairs.
+            const float4 *sg4 = reinterpret_cast<const float4 *>(sgain);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                if (c == 0 ? rot0 : rot1) continue;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {   // chunks c and c + 2
+                    const int lc = 4 * (c + 2 * h) + tq;
+                    const float4 gv[2] = {sg4[2 * gchunk(lc)], sg4[2 * gchunk(lc) + 1]};
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        uint32_t &w = qb[2 * (c + 2 * h) + (qq >> 1)][qq & 1];
+                        const float2 v = fmul2(make_float2(bf16lo(w), bf16hi(w)), gain_pair(gv, qq));
+                        w = pack_bf16x2(v.x, v.y);
+                    }
+                }
+            }
+        }
     }
 
     float o[8][4];
@@ -431,16 +447,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                         rotate_word(bl.k1[c], bl.k1[c + 2], qq, stg[(8 + 4 * c + qq) * 32 + sw]);
                     }
                 }
-            } else if constexpr (SHARED) {
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const float2 ga = gain_pair(gA, qq), gb = gain_pair(gB, qq);
-                    gain_word(bl.k0[c], qq, ga);
-                    gain_word(bl.k0[c + 2], qq, gb);
-                    gain_word(bl.k1[c], qq, ga);
-                    gain_word(bl.k1[c + 2], qq, gb);
-                }
             }
+            // (a group that never rotates has its gain on the query: raw keys)
         }
         // S^T (16 keys x 8 heads) in two independent accumulation chains
         float s[4] = {0.f, 0.f, 0.f, 0.f}, t[4] = {0.f, 0.f, 0.f, 0.f};

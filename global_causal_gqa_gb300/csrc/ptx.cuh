@@ -67,7 +67,7 @@ __device__ __forceinline__ bool in_bounds(long i, long n, int *status, int site)
 #define GQA_IN_BOUNDS(i, n, status, site) \
     ::gqa::in_bounds(static_cast<long>(i), static_cast<long>(n), (status), (site))
 #else
-#define GQA_IN_BOUNDS(i, n, status, site) true
+#define GQA_IN_BOUNDS(i, n, status, site) ((void)(n), true)
 #endif
 
 // ---- mbarrier ---------------------------------------------------------------------
