@@ -411,17 +411,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         issue_pv(i, vst, j > 0);
                         if (j == n - 1) umma_commit(&bars->o_final[i]);
-                        // slots whose last reader has been issued, released here rather
-                        // than between a score product and the next PV product: K(j)
-                        // (read by S_1(j), issued in the previous step) and V(j)
-                        if (i == 0 && j > 0) umma_commit(&bars->empty[kprev]);
-                        if (i == ntile - 1) umma_commit(&bars->empty[vst]);
                         if (j + 1 < n) {
                             if (i == 0) take_k(kst);
                             if (!ok) break;
                             // S_i(j+1) overwrites the columns P_i(j) sits in
                             wait_last_pv(i, 5);
+                            // PV_i(j) has completed, and with it every earlier product of
+                            // this thread: K(j) (read by S_0(j) and S_1(j)) is free once
+                            // PV_0(j) is, V(j) once the last tile's PV(j) is.  Plain arrivals
+                            // here cost the issuing thread less than commits.
+                            if (i == 0 && j > 0) mbar_arrive(&bars->empty[kprev]);
+                            if (i == ntile - 1) mbar_arrive(&bars->empty[vst]);
                             if (ok) issue_s(qaddr[i], i, kst);
+                        } else {
+                            // the item's last key tile: K and V go free when its products do
+                            if (i == 0 && j > 0) umma_commit(&bars->empty[kprev]);
+                            if (i == ntile - 1) umma_commit(&bars->empty[vst]);
                         }
                     }
                     kprev = kst;
