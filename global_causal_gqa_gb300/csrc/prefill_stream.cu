@@ -235,15 +235,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = mbar_wait(&bars->p_full[i], j & 1))) break;
                     tc_fence_after();
                     issue_pv(i, s, j > 0);
-                    if (i == ntile - 1) umma_commit(&bars->kv_empty[s]);
                     if (j + 1 < n_tiles) {
                         if (i == 0 && !(ok = mbar_wait(&bars->k_full[s1], par1))) break;
                         // S_i(j+1) overwrites the TMEM columns P_i(j) sits in; the tensor
                         // pipe does not order that write after PV_i(j)'s read, so wait for
                         // PV_i(j) to complete first
                         if (!(ok = mbar_wait(&bars->o_done[i], j & 1))) break;
+                        // with the last tile's PV(j), every product that read stage s has
+                        // completed: a plain arrival frees it (cheaper than a commit)
+                        if (i == ntile - 1) mbar_arrive(&bars->kv_empty[s]);
                         tc_fence_after();
                         issue_s(i, s1);
+                    } else if (i == ntile - 1) {
+                        umma_commit(&bars->kv_empty[s]);
                     }
                 }
             }
