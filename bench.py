@@ -332,23 +332,29 @@ def e2e_prefill(L, st, steps, warmup, stream, flops):
     step is cut into independent chunks (a batch element and one KV head with its query
     group), each one gqa_attn_prefill call on the caller's stream; later chunks' inputs
     copy in on one stream and earlier chunks' outputs copy out on another while a chunk
-    computes, as a serving loop would overlap its transfers.  Measured on the local
+    computes, as a serving loop would overlap its transfers.  The host inputs are laid out
+    chunk after chunk (a chunk's Q heads, K and V side by side, as a serving loop would
+    gather a request's tensors), so each chunk comes in with one copy; the device tensors
+    have the same layout and each call gets its chunk's pointers.  Measured on the local
     prefill: 246 TFLOP/s with the copies and the whole call in series, 389 / 411 / 414
-    with 4 / 8 / 16 chunks (the copies then bound the step)."""
+    with 4 / 8 / 16 chunks and three copies per chunk."""
     import torch
     import global_causal_gqa_gb300 as gqa
     x = st["x"]
-    qh, kh, vh = (t.pin_memory() for t in (x.q, x.k, x.v))
-    oh = torch.empty_like(x.q).pin_memory()
     G = L.Hq // L.Hkv
-    hs = 1   # KV heads per chunk
-    parts = [(b, g0) for b in range(L.B) for g0 in range(0, L.Hkv, hs)]
+    parts = [(b, g) for b in range(L.B) for g in range(L.Hkv)]
+    qn, kn = G * L.T * L.d, L.S * L.d          # elements of a chunk's Q and of its K (= V)
+    cn = qn + 2 * kn
+    hin = torch.empty(len(parts) * cn, dtype=torch.bfloat16).pin_memory()
+    for c, (b, g) in enumerate(parts):
+        hin[c * cn: c * cn + qn].copy_(x.q[b, G * g: G * (g + 1)].reshape(-1))
+        hin[c * cn + qn: c * cn + qn + kn].copy_(x.k[b, g].reshape(-1))
+        hin[c * cn + qn + kn: (c + 1) * cn].copy_(x.v[b, g].reshape(-1))
+    din = torch.empty_like(hin, device="cuda")
+    oh = torch.empty_like(x.q).pin_memory()
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
     timer = Timer(torch, stream, 2)
     whole = st["o"].clone()   # the device-timed single call's output, same inputs
-
-    def qs(t, b, g0):
-        return t[b, G * g0:G * (g0 + hs)]
 
     def step(mark):
         mark()
@@ -358,24 +364,24 @@ def e2e_prefill(L, st, steps, warmup, stream, flops):
         d2h.wait_event(start)
         landed = []
         with torch.cuda.stream(h2d):
-            for b, g0 in parts:
-                qs(st["q"], b, g0).copy_(qs(qh, b, g0), non_blocking=True)
-                st["k"][b, g0:g0 + hs].copy_(kh[b, g0:g0 + hs], non_blocking=True)
-                st["v"][b, g0:g0 + hs].copy_(vh[b, g0:g0 + hs], non_blocking=True)
+            for c in range(len(parts)):
+                din[c * cn: (c + 1) * cn].copy_(hin[c * cn: (c + 1) * cn], non_blocking=True)
                 e = torch.cuda.Event()
                 e.record(h2d)
                 landed.append(e)
-        for (b, g0), e in zip(parts, landed):
+        for c, ((b, g), e) in enumerate(zip(parts, landed)):
             stream.wait_event(e)
-            gqa.gqa_attn_prefill(qs(st["q"], b, g0), st["k"][b, g0:g0 + hs],
-                                 st["v"][b, g0:g0 + hs], qs(st["o"], b, g0), None, 1, L.T, L.S,
-                                 G * hs, hs, L.d, L.window, L.scale, st["table"], L.S, 0,
-                                 st["ws"], st["wsb"], stream)
+            qd = din[c * cn: c * cn + qn]
+            kd = din[c * cn + qn: c * cn + qn + kn]
+            vd = din[c * cn + qn + kn: (c + 1) * cn]
+            od = st["o"][b, G * g: G * (g + 1)]
+            gqa.gqa_attn_prefill(qd, kd, vd, od, None, 1, L.T, L.S, G, 1, L.d, L.window,
+                                 L.scale, st["table"], L.S, 0, st["ws"], st["wsb"], stream)
             done = torch.cuda.Event()
             done.record(stream)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(done)
-                qs(oh, b, g0).copy_(qs(st["o"], b, g0), non_blocking=True)
+                oh[b, G * g: G * (g + 1)].copy_(od, non_blocking=True)
         out = torch.cuda.Event()
         out.record(d2h)
         stream.wait_event(out)
@@ -388,9 +394,10 @@ def e2e_prefill(L, st, steps, warmup, stream, flops):
         raise SystemExit("end-to-end chunked output differs from the single call's")
     nb = lambda t: t.numel() * t.element_size()  # noqa: E731
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": nb(qh) + nb(kh) + nb(vh), "d2h_bytes_per_step": nb(oh),
+            "h2d_bytes_per_step": nb(hin), "d2h_bytes_per_step": nb(oh),
             "pipeline": f"{len(parts)} public calls per step (batch element x KV head), "
-                        "copies in and out on two more streams overlapping the compute"}
+                        "one copy in per call (its Q, K and V side by side) and one out, on "
+                        "two more streams overlapping the compute"}
 
 
 # ----------------------------------------------------------------------------------------
