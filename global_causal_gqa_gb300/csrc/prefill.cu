@@ -21,7 +21,8 @@
 // current item's epilogue overlaps the next item's first score products.
 //
 // Warp roles (12 warps, 3 warpgroups; 3 warps per SM sub-partition cap every thread at
-// 168 registers):
+// 168 registers at launch, and warpgroup 0 then hands registers to the two softmax
+// warpgroups: 96 and 200 per thread):
 //   warp 0      TMA producer: Q tiles of each item into Q buffer (item & 1), K and V
 //               tiles into a 3-slot ring in the order they are consumed:
 //               K(0), V(0), K(1), V(1), ...
