@@ -47,6 +47,7 @@ constexpr int kMaxSlots = 5;
 
 struct WBars {
     uint64_t q_full, q_ready;
+    uint64_t t_full;          // the Q rows' RoPE table rows, staged in ring slots 1..4
     uint64_t full[kMaxSlots], empty[kMaxSlots];
     uint64_t s_full[2], p_full[2], o_done, mma_done;
     // the last PV product: S(j+2) waits only for PV(j), so when the softmax finishes the
@@ -111,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->t_full, 1);
         mbar_init(&bars->q_ready, kThreads);
         for (int i = 0; i < NS; ++i) {
             mbar_init(&bars->full[i], 1);
@@ -187,30 +189,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(dst + BOX, map, &bars->full[st], c0 + 64, n0, zk);
         ++pu;
     };
+    // The Q rows' table rows (positions q_lo .. q_hi, D/2 (cos, sin) pairs each: 128 KB at
+    // D = 256) are staged by bulk copies in ring slots 1..4, which the K/V stream only
+    // needs after the rotation: the rotation then reads them from shared memory instead of
+    // waiting on L2 row by row.
+    constexpr int kTabRowBytes = D * 4;
+    static_assert(kBM * kTabRowBytes <= (NS - 1) * kSlotBytes, "table rows fit in the ring");
+    const int n_tab_rows = q_hi - q_lo + 1;
+    uint8_t *stab = smem + OFF_RING + kSlotBytes;
     if (warp == 0 && lane == 0) {
-        // Q, then the ring loads that need no free slot, before the rotation below
+        // Q, the table rows and the first ring load, before the rotation below
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         mbar_arrive_expect_tx(&bars->q_full, QBYTES);
         for (int i = 0; i < D / 64; ++i)
             tma_load_3d(sQ + i * QBOX, &tmQ, &bars->q_full, 64 * i, mb * kBM, b * p.Hq + h);
-        while (pu < min(NS, n_loads)) put();
+        mbar_arrive_expect_tx(&bars->t_full, n_tab_rows * kTabRowBytes);
+        for (int r0 = 0; r0 < n_tab_rows; r0 += 32)
+            bulk_copy_g2s(stab + r0 * kTabRowBytes,
+                          p.table + (size_t)(q_lo + r0) * (D / 2),
+                          min(32, n_tab_rows - r0) * kTabRowBytes, &bars->t_full);
+        if (n_loads > 0) put();   // slot 0; slots 1..4 once the rotation is done
     }
 
     // ================= RoPE on the Q tile, by every warp =================
     // Warp w takes rows QR w .. QR w + QR - 1, one row at a time: lane l rotates pairs
     // 64 bb + 2l, 64 bb + 2l + 1 of every 64-pair box bb against their partners D/2 later
-    // (the same swizzled word of box bb + NB).  The table row is read as NB coalesced
-    // 512-byte pieces, RIF rows in flight.
+    // (the same swizzled word of box bb + NB).  The table row is read from its staging in
+    // the ring as NB 512-byte pieces, RIF rows at a time.
     {
         constexpr int NB = D / 128;               // 64-pair boxes in each half of a row
         constexpr int QR = kBM / (kThreads / 32);   // rows per warp
         constexpr int RIF = QR < 32 / NB ? QR : 32 / NB;   // rows whose table loads are in flight
-        bool qok = warp_wait_w(&bars->q_full, 0);
+        bool qok = warp_wait_w(&bars->q_full, 0) && warp_wait_w(&bars->t_full, 0);
         if (!qok) set_timeout(p.status, kDiagPrefillWide, 3, 8, 0);
         if (qok) {
-            const float4 *t4 = reinterpret_cast<const float4 *>(p.table);
+            const float4 *t4 = reinterpret_cast<const float4 *>(stab);
             for (int r0 = 0; r0 < QR; r0 += RIF) {
                 float4 tv[RIF][NB];
 #pragma unroll
@@ -220,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int pos = min(p.S - p.T + mb * kBM + row, p.S - 1);
 #pragma unroll
                     for (int bb = 0; bb < NB; ++bb)
-                        tv[i][bb] = __ldg(t4 + (size_t)pos * (D / 4) + 32 * bb + lane);
+                        tv[i][bb] = t4[(size_t)(pos - q_lo) * (D / 4) + 32 * bb + lane];
                 }
 #pragma unroll
                 for (int i = 0; i < RIF; ++i) {
@@ -248,10 +263,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ================= TMA producer: the rest of the ring =================
         if (lane == 0) {
+            // the table rows in slots 1..4 have been read once every thread has arrived
+            pok = mbar_wait(&bars->q_ready, 0);
+            if (!pok) set_timeout(p.status, kDiagPrefillWide, 0, 2, 0);
             while (pok && pu < n_loads) put();
             if (!pok) set_status(p.status, GQA_ERR_DEVICE_TIMEOUT);
             // never leave the CTA with copies in flight
             mbar_wait(&bars->q_full, 0);
+            mbar_wait(&bars->t_full, 0);
             for (int w = max(0, pu - NS); w < pu; ++w) mbar_wait(&bars->full[w % NS], (w / NS) & 1);
         }
         __syncwarp();
